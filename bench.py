@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""Benchmark of the 8-bit block-wise dynamic Adam step on GB300.
+
+One step = one multi-tensor 8-bit Adam step over the whole synthetic
+parameter set (default: the Llama-2-7B-shaped set, 291 tensors, 6.74e9 fp32
+parameters, bf16 gradients, u8 codes + fp32 absmax per 2048 block).  The
+metric is parameters updated per second (whole job, all ranks); the roofline
+object reports the fused kernel's achieved HBM bandwidth from its algorithmic
+bytes per parameter.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on host cores
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU (weak scaling; the step has no exchange), the timed region is
+bracketed by barriers and the slowest rank's time is reported.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "8-bit blockwise Adam params updated/sec and achieved HBM GB/s (% of GB300 peak)"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 126 * 2 ** 20
+
+
+def algorithmic_bytes_per_param(grad_bytes: int) -> float:
+    """p read+write 8, g read, m and v codes read+write 2 + 2, and the two
+    fp32 absmax per 2048 block read+write (16 B / 2048)."""
+    return 8 + grad_bytes + 4 + 16.0 / 2048
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama2_7b", choices=["llama2_7b", "gpt_350m", "ragged_2000", "adam_1m"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+        self.first = threading.Event()
+
+    def start(self, wait_s=3.0):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        self.first.wait(wait_s)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.perf_counter(), parts))
+                self.first.set()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(2)
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.rows if t0 <= t <= t1] or [r for (_, r) in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_per_param():
+    """DRAM bytes per parameter of the fused kernel from the committed ncu
+    summary, valid only while the kernel source is the one profiled."""
+    src = os.path.join(ROOT, "block_wise_dynamic_gb300", "csrc", "kernels.cu")
+    prof = os.path.join(ROOT, "profiles", "adam8bit_kernel_llama2_7b.md")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        kv = {}
+        for line in open(prof):
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                kv[k.strip()] = v.strip().strip("`")
+        if kv.get("kernels.cu sha256[:16]") != sha:
+            return None
+        return float(kv["dram bytes per param"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def host_mem_available() -> int:
+    try:
+        with open("/proc/meminfo") as fh:
+            for line in fh:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+# --------------------------------------------------------------------------
+# the oracle on host cores
+
+def oracle_rate(n_params: int, steps: int, warm: int = 1):
+    """Params/s of the CPU oracle's 8-bit Adam step over a sample of n_params
+    (whole 2048 blocks of N(0, 0.02) params, bf16 N(0, 1e-3) grads)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from oracle.adam import widen_bf16
+    from block_wise_dynamic_gb300 import workloads as W
+
+    p = W.gen_normal(n_params, 0.02, seed=0).numpy()
+    g = W.gen_normal(n_params, 1e-3, seed=1, dtype=torch.bfloat16)
+    g = widen_bf16(g.view(torch.int16).numpy().view(np.uint16))
+    st = oracle.state_init(n_params)
+    oracle.adam8bit_step(p[:2048], g[:2048], *oracle.state_init(2048), oracle.AdamHParams(step=1))
+    t = 0
+    for _ in range(warm):
+        t += 1
+        p, *st = oracle.adam8bit_step(p, g, *st, oracle.AdamHParams(step=t))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        t += 1
+        p, *st = oracle.adam8bit_step(p, g, *st, oracle.AdamHParams(step=t))
+    dt = time.perf_counter() - t0
+    return n_params * steps / dt, dt
+
+
+def cpu_baseline_leg():
+    n = 8192 * 2048
+    rate, dt = oracle_rate(n, steps=2, warm=0)
+    return {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
+            "sample": f"2 steps of the oracle on {n} params (8192 blocks) of the same distributions, "
+                      f"{dt:.1f} s, single process (NumPy element-wise ops are single-threaded)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return
+    n = 1024 * 2048
+    rate, dt = oracle_rate(n, steps=args.steps, warm=args.warmup)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "params/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "sample_params_per_step": n},
+        "cpu_baseline": {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: the oracle's 8-bit Adam step on {n} params (1024 blocks) "
+                                   f"of the {args.workload} distributions, single process"},
+        "e2e": {"value": rate, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# the GPU path
+
+def run_ours(args):
+    import torch
+
+    import block_wise_dynamic_gb300 as bwd
+    from block_wise_dynamic_gb300 import workloads as W
+
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    bwd.init(dev)
+
+    wl = W.workload(args.workload)
+    sizes = [n for n in wl.sizes if n > 0]
+    N = sum(sizes)
+    gbytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
+    bpp = algorithmic_bytes_per_param(gbytes)
+
+    ps, gs, sts = [], [], []
+    for i, n in enumerate(sizes):
+        ps.append(W.gen_normal(n, 0.02, seed=rank * 1_000_003 + i, device=dev))
+        gs.append(W.gen_normal(n, wl.grad_std[i], seed=rank * 1_000_003 + 500_000 + i, device=dev,
+                               dtype=wl.grad_dtype))
+        sts.append(bwd.state_init(n, dev))
+    mt = bwd.MultiTensorArgs(ps, gs, *[[s[k] for s in sts] for k in range(4)])
+    launches_per_step = math.ceil(len(sizes) / 448)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps)
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        mt.step(step=t, **hp)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    c0 = time.perf_counter()
+    e0.record(stream)
+    for k in range(args.steps):
+        t += 1
+        ev[k][0].record(stream)
+        mt.step(step=t, **hp)
+        ev[k][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    c1 = time.perf_counter()
+    clocks.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+
+    # end to end through the public API with host buffers: the step's
+    # gradients arrive from pinned host memory and the updated parameters go
+    # back to it, copies inside the timed region
+    e2e = None
+    pinned_bytes = N * (gbytes + 4)
+    if args.e2e_steps > 0 and host_mem_available() < 2 * pinned_bytes * max(world, 1):
+        e2e = {"value": None, "unit": "params/s", "h2d_bytes_per_step": N * gbytes, "d2h_bytes_per_step": N * 4,
+               "skipped": f"needs {pinned_bytes / 1e9:.0f} GB of pinned host memory per rank"}
+    elif args.e2e_steps > 0:
+        gh = torch.empty(N, dtype=wl.grad_dtype, pin_memory=True)
+        ph = torch.empty(N, dtype=torch.float32, pin_memory=True)
+        off = 0
+        ghv, phv = [], []
+        for i, n in enumerate(sizes):
+            ghv.append(gh[off:off + n])
+            phv.append(ph[off:off + n])
+            ghv[-1].copy_(gs[i])
+            off += n
+        torch.cuda.synchronize(dev)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(dev)
+        f0.record(stream)
+        for _ in range(args.e2e_steps):
+            t += 1
+            for i in range(len(sizes)):
+                gs[i].copy_(ghv[i], non_blocking=True)
+            mt.step(step=t, **hp)
+            for i in range(len(sizes)):
+                phv[i].copy_(ps[i], non_blocking=True)
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_ms = f0.elapsed_time(f1)
+        if world > 1:
+            tt = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        e2e = {"value": world * N * args.e2e_steps / (e2e_ms / 1e3), "unit": "params/s",
+               "h2d_bytes_per_step": N * gbytes, "d2h_bytes_per_step": N * 4,
+               "steps": args.e2e_steps,
+               "what": "per step: H2D of all gradients from pinned host memory, the multi-tensor step, "
+                       "D2H of all updated fp32 parameters into pinned host memory, one stream"}
+        del gh, ph, ghv, phv
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    value = world * N * args.steps / (elapsed_ms / 1e3)
+    mean_launch_ms = statistics.fmean(launch_ms) / launches_per_step
+    peak, peak_kind = measured_peak()
+    achieved = bpp * N / launches_per_step / (mean_launch_ms / 1e3) / 1e9
+    tpp = traffic_per_param()
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "params/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": wl.name,
+            "params": N,
+            "tensors": len(sizes),
+            "grad_dtype": "bf16" if gbytes == 2 else "f32",
+            "state": "u8 codes (signed m, unsigned v) + f32 absmax per 2048 block",
+            "l2": f"inputs larger than L2 ({bpp * N / 1e9:.1f} GB per step vs {L2_BYTES / 2**20:.0f} MiB L2), no flush",
+            "parallelism": f"replica per GPU x{world}",
+        },
+        "hbm_gbs": bpp * N / (elapsed_ms / args.steps / 1e3) / 1e9,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "adam8bit_kernel<bf16>" if gbytes == 2 else "adam8bit_kernel<f32>",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (copy bandwidth)",
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": None if tpp is None else tpp * N / launches_per_step,
+            "bytes_per_param": bpp,
+            "mean_launch_ms": mean_launch_ms,
+        },
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clocks.summary(c0, c1),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_leg()
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,94 @@
+"""Drop-in replacement for ``torch.optim.Adam`` with 8-bit block-wise states.
+
+The page on "8-BIT OPTIMIZERS VIA BLOCK-WISE QUANTIZATION" says switching to
+the 8-bit optimizer takes two lines of code (introduction and 总结); this
+class is that switch:
+
+    from block_wise_dynamic_gb300 import Adam8bit
+    opt = Adam8bit(model.parameters(), lr=1e-3, betas=(0.9, 0.999), eps=1e-8)
+
+Parameters must be fp32 CUDA tensors (master weights); gradients fp32 or
+bf16.  Per parameter the state holds ``step`` and the codes and absmax of
+both moments; ``state_dict()`` / ``load_state_dict()`` round-trip them
+exactly.  Each ``step()`` issues one multi-tensor launch per (device,
+gradient dtype, step count) group.
+"""
+
+from __future__ import annotations
+
+from collections import defaultdict
+
+import torch
+
+from . import MultiTensorArgs, num_blocks, state_init
+
+
+class Adam8bit(torch.optim.Optimizer):
+    def __init__(self, params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.0):
+        if lr < 0.0:
+            raise ValueError(f"invalid learning rate {lr}")
+        if not (0.0 <= betas[0] < 1.0 and 0.0 <= betas[1] < 1.0):
+            raise ValueError(f"invalid betas {betas}")
+        if eps < 0.0:
+            raise ValueError(f"invalid eps {eps}")
+        if weight_decay != 0.0:
+            raise ValueError("weight_decay is not supported by this step")
+        super().__init__(params, dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay))
+        self._args_cache = {}
+
+    def _state_for(self, p: torch.Tensor):
+        st = self.state[p]
+        if len(st) == 0:
+            mc, ma, vc, va = state_init(p.numel(), p.device)
+            st["step"] = 0
+            st["m_codes"], st["m_absmax"], st["v_codes"], st["v_absmax"] = mc, ma, vc, va
+        return st
+
+    @torch.no_grad()
+    def step(self, closure=None):
+        loss = None
+        if closure is not None:
+            with torch.enable_grad():
+                loss = closure()
+        for gi, group in enumerate(self.param_groups):
+            buckets = defaultdict(list)
+            for p in group["params"]:
+                if p.grad is None:
+                    continue
+                if p.dtype != torch.float32 or not p.is_cuda:
+                    raise TypeError("Adam8bit needs fp32 CUDA parameters")
+                if p.grad.is_sparse:
+                    raise TypeError("sparse gradients are not supported")
+                st = self._state_for(p)
+                if st["m_absmax"].numel() != num_blocks(p.numel()):
+                    raise ValueError("state does not match the parameter size")
+                st["step"] += 1
+                buckets[(p.device, p.grad.dtype, st["step"])].append(p)
+            b1, b2 = group["betas"]
+            for (dev, gdt, t), ps in buckets.items():
+                grads = [q.grad if q.grad.is_contiguous() else q.grad.contiguous() for q in ps]
+                sts = [self.state[q] for q in ps]
+                key = (gi, dev, gdt)
+                ptrs = tuple(x.data_ptr() for x in ps) + tuple(x.data_ptr() for x in grads)
+                cached = self._args_cache.get(key)
+                if cached is None or cached[0] != ptrs:
+                    args = MultiTensorArgs(
+                        [q.view(-1) for q in ps], [x.view(-1) for x in grads],
+                        [s["m_codes"] for s in sts], [s["m_absmax"] for s in sts],
+                        [s["v_codes"] for s in sts], [s["v_absmax"] for s in sts],
+                    )
+                    self._args_cache[key] = (ptrs, args)
+                else:
+                    args = cached[1]
+                args.step(lr=group["lr"], beta1=b1, beta2=b2, eps=group["eps"], step=t)
+        return loss
+
+    def load_state_dict(self, state_dict):
+        self._args_cache = {}
+        super().load_state_dict(state_dict)
+        # torch casts every floating parameter's state tensors to the
+        # parameter dtype; codes are integers 0..255, so casting back is exact
+        for st in self.state.values():
+            for k in ("m_codes", "v_codes"):
+                if k in st and st[k].dtype != torch.uint8:
+                    st[k] = st[k].to(torch.uint8)

@@ -1,0 +1,158 @@
+/*
+ * bwd.h -- C ABI of the GB300 (sm_103a) 8-bit block-wise dynamic Adam library.
+ *
+ * The method: "8-BIT OPTIMIZERS VIA BLOCK-WISE QUANTIZATION", as summarised on
+ * wiki.neutronadmin.com/news/16836.  Adam's two moments (section 一) are kept
+ * as 8-bit codes; for the update they are dequantized to fp32, the update
+ * runs, and they are quantized again (section 二, opening paragraph).  Codes
+ * index a 256-entry dynamic-tree map (section 二 / 动态量化: sign, zero-run
+ * exponent, indicator bit, linear fraction; the second moment uses the
+ * unsigned variant whose sign bit is one more fraction bit), and every block
+ * of 2048 elements carries one fp32 absmax (section 二 / 逐块量化).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named "device" are CUDA device (or managed) memory of the
+ *     CURRENT device; the caller owns them.  The library keeps only its own
+ *     immutable code tables (about 9 KB per device, uploaded on first use).
+ *   - Every device operation is enqueued on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and returns without waiting for it.  Launch
+ *     errors are reported as BWD_ERR_CUDA; faults inside a kernel surface on
+ *     the caller's next synchronisation, as for any CUDA work.
+ *   - Arguments are checked on the host before anything is enqueued; a
+ *     rejected call has no effect.  n == 0 is a successful no-op.
+ *   - Any alignment is accepted.  16-byte aligned pointers (and, per tensor,
+ *     full 2048-element blocks) take the vectorised path; other blocks take
+ *     an element-wise path with identical results.
+ *   - Input and output ranges must not overlap, except where an argument is
+ *     documented as updated in place.
+ *   - Non-finite inputs are outside the method; they never cause an
+ *     out-of-bounds access but their codes are unspecified.
+ *   - The first call on a device uploads the tables with a blocking copy, so
+ *     it must not happen during CUDA stream capture; bwd_init() does it
+ *     explicitly.
+ *   - Entry points are thread-safe; bwd_last_error() is per thread.
+ */
+#ifndef BWD_H
+#define BWD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Elements per quantization block (section 二 / 逐块量化). */
+#define BWD_BLOCK 2048
+
+typedef enum {
+  BWD_OK = 0,
+  BWD_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum, ... */
+  BWD_ERR_UNSUPPORTED_DTYPE = 2, /* gradient dtype not in bwd_dtype          */
+  BWD_ERR_CUDA = 3               /* a CUDA runtime call or launch failed      */
+} bwd_status;
+
+/* Which dynamic-tree map (section 二 / 动态量化). */
+typedef enum {
+  BWD_MAP_SIGNED = 0,   /* sign + zero-run exponent + indicator + fraction  */
+  BWD_MAP_UNSIGNED = 1  /* the sign bit reused as fraction (second moment)  */
+} bwd_map_kind;
+
+/* Gradient element types. */
+typedef enum { BWD_F32 = 0, BWD_BF16 = 1 } bwd_dtype;
+
+/* Adam hyper-parameters (section 一: first and second moment).  `step` is
+ * the 1-based index t of the step being taken (bias corrections use it);
+ * weight_decay must be 0. */
+typedef struct {
+  float lr;
+  float beta1;
+  float beta2;
+  float eps;
+  float weight_decay;
+  int64_t step;
+} bwd_adam_hparams;
+
+/* Number of 2048-element blocks of an n-element tensor: ceil(n / 2048).
+ * Returns -1 for n < 0. */
+int64_t bwd_num_blocks(int64_t n);
+
+/* Host only.  Writes the 256-entry map of `kind` in ascending order (a code
+ * is an index into it; the signed map holds -0.0 at 127 and +0.0 at 128) and
+ * the 255 decision thresholds, threshold i being the binary32 value nearest
+ * to the midpoint of entries i and i+1.  Magnitudes follow the dynamic-tree
+ * layout of section 二 / 动态量化 with a decimal zero-run exponent and a
+ * linear fraction grid on (0.1, 1] per decade.  Either output may be NULL. */
+bwd_status bwd_build_map(bwd_map_kind kind, float* map_out /*[256]*/,
+                         float* thresholds_out /*[255]*/);
+
+/* Uploads the code tables to the current device if not done yet (blocking).
+ * Optional: every entry point below does it on first use. */
+bwd_status bwd_init(void);
+
+/* Block-wise quantization (section 二 / 逐块量化 and 动态量化).
+ *   x      : device, float[n], read only.
+ *   codes  : device, uint8[n], written: index of the nearest map entry to
+ *            x / absmax (binary32 IEEE division; a value exactly on a
+ *            threshold takes the higher code; +-0 take the code of +0).
+ *   absmax : device, float[ceil(n/2048)], written: max |x| of each block
+ *            (the last block may be partial).  A block whose absmax is 0
+ *            gets the code of +0.0 everywhere. */
+bwd_status bwd_quantize_blockwise(const float* x, int64_t n, bwd_map_kind kind,
+                                  uint8_t* codes, float* absmax, void* stream);
+
+/* Block-wise dequantization (section 一: back from codes to values).
+ *   codes  : device, uint8[n]; absmax: device, float[ceil(n/2048)].
+ *   y      : device, float[n], written: map[code] * absmax[block] (one
+ *            binary32 multiply). */
+bwd_status bwd_dequantize_blockwise(const uint8_t* codes, const float* absmax,
+                                    int64_t n, bwd_map_kind kind, float* y,
+                                    void* stream);
+
+/* State before the first step: m codes := code of +0.0 in the signed map,
+ * v codes := code of 0 in the unsigned map, both absmax := 0.
+ *   m_codes, v_codes : device uint8[n];  m_absmax, v_absmax : device
+ *   float[ceil(n/2048)].  All written. */
+bwd_status bwd_state_init(uint8_t* m_codes, float* m_absmax, uint8_t* v_codes,
+                          float* v_absmax, int64_t n, void* stream);
+
+/* One 8-bit Adam step on one flat tensor (section 二, opening paragraph):
+ * dequantize m (signed map) and v (unsigned map), run Adam in fp32,
+ *     m = b1 m + (1-b1) g;  v = b2 v + ((1-b2) g) g;
+ *     p = p - (s m) / (sqrt(v) / c + eps),
+ * with s = fp32(lr / (1 - b1^t)) and c = fp32(sqrt(1 - b2^t)) formed in
+ * binary64 on the host, each element operation one binary32 rounding in
+ * that order; then requantize m and v block by block with fresh absmax.
+ *   p                : device float[n], updated in place.
+ *   g                : device, float[n] or bf16[n] per g_dtype, read only.
+ *   m_codes, v_codes : device uint8[n], updated in place.
+ *   m_absmax,v_absmax: device float[ceil(n/2048)], updated in place.
+ *   hp               : host pointer; hp->step >= 1, weight_decay == 0. */
+bwd_status bwd_adam8bit_step(float* p, const void* g, bwd_dtype g_dtype,
+                             uint8_t* m_codes, float* m_absmax,
+                             uint8_t* v_codes, float* v_absmax, int64_t n,
+                             const bwd_adam_hparams* hp, void* stream);
+
+/* The same step over a list of tensors in as few launches as the kernel
+ * parameter space allows (448 tensors per launch).  Blocks never span two
+ * tensors.  All arrays are HOST arrays of length num_tensors holding device
+ * pointers (or sizes); each tensor follows the single-tensor contract above.
+ * Tensors with n == 0 are skipped; num_tensors == 0 is a no-op. */
+bwd_status bwd_adam8bit_step_multi(int32_t num_tensors, float* const* p,
+                                   const void* const* g, bwd_dtype g_dtype,
+                                   uint8_t* const* m_codes,
+                                   float* const* m_absmax,
+                                   uint8_t* const* v_codes,
+                                   float* const* v_absmax, const int64_t* n,
+                                   const bwd_adam_hparams* hp, void* stream);
+
+/* Static description of a status code. */
+const char* bwd_status_string(bwd_status status);
+
+/* Detail of the last failed call on this thread ("" if none). */
+const char* bwd_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BWD_H */

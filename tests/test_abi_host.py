@@ -1,0 +1,111 @@
+"""The C-ABI library: it loads, exports what include/bwd.h declares, its host
+codebook builder agrees with the oracle bit for bit, and it rejects bad
+arguments on the host before touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_wise_dynamic_gb300 import build as b
+
+    b.build()
+    from block_wise_dynamic_gb300 import _abi
+
+    return _abi.load()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(bwd_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("bwd_quantize_blockwise", "bwd_dequantize_blockwise", "bwd_adam8bit_step",
+                 "bwd_adam8bit_step_multi", "bwd_build_map", "bwd_state_init"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+@pytest.mark.parametrize("kind,signed", [(0, True), (1, False)])
+def test_host_builder_matches_oracle_bitwise(lib, kind, signed):
+    m = np.empty(256, np.float32)
+    t = np.empty(255, np.float32)
+    assert lib.bwd_build_map(kind, m.ctypes.data, t.ctypes.data) == 0
+    assert np.array_equal(m.view(np.uint32), oracle.dynamic_map(signed).view(np.uint32))
+    assert np.array_equal(t.view(np.uint32), oracle.thresholds(signed).view(np.uint32))
+    assert lib.bwd_build_map(kind, None, None) == 0
+
+
+def test_num_blocks(lib):
+    for n, nb in [(0, 0), (1, 1), (2047, 1), (2048, 1), (2049, 2), (6_738_415_616, 3_290_242)]:
+        assert lib.bwd_num_blocks(n) == nb
+    assert lib.bwd_num_blocks(-1) == -1
+
+
+def test_status_strings(lib):
+    assert lib.bwd_status_string(0) == b"ok"
+    assert lib.bwd_status_string(1) == b"invalid argument"
+    assert lib.bwd_status_string(99) == b"unknown status"
+
+
+def test_bad_arguments_are_rejected_on_the_host(lib):
+    from block_wise_dynamic_gb300._abi import AdamHParams
+
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: rejected first
+    assert lib.bwd_build_map(7, None, None) == 1
+    assert lib.bwd_quantize_blockwise(fake, -1, 0, fake, fake, None) == 1
+    assert lib.bwd_quantize_blockwise(fake, 10, 5, fake, fake, None) == 1
+    assert lib.bwd_quantize_blockwise(None, 10, 0, fake, fake, None) == 1
+    assert b"NULL" in lib.bwd_last_error()
+    assert lib.bwd_dequantize_blockwise(fake, None, 10, 0, fake, None) == 1
+    assert lib.bwd_state_init(fake, fake, None, fake, 10, None) == 1
+    # n == 0 is a no-op that succeeds without a device
+    assert lib.bwd_quantize_blockwise(None, 0, 0, None, None, None) == 0
+    assert lib.bwd_dequantize_blockwise(None, None, 0, 1, None, None) == 0
+    assert lib.bwd_state_init(None, None, None, None, 0, None) == 0
+
+    hp = AdamHParams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1)
+    step = lib.bwd_adam8bit_step
+    assert step(fake, fake, 0, fake, fake, fake, fake, 0, ctypes.byref(hp), None) == 0
+    assert step(fake, fake, 7, fake, fake, fake, fake, 10, ctypes.byref(hp), None) == 2
+    assert step(fake, fake, 0, fake, fake, fake, fake, 10, None, None) == 1
+    for bad in (AdamHParams(1e-3, 0.9, 0.999, 1e-8, 0.0, 0),      # step 0
+                AdamHParams(1e-3, 1.0, 0.999, 1e-8, 0.0, 1),      # beta1 = 1
+                AdamHParams(1e-3, 0.9, -0.1, 1e-8, 0.0, 1),       # beta2 < 0
+                AdamHParams(float("nan"), 0.9, 0.999, 1e-8, 0.0, 1),
+                AdamHParams(1e-3, 0.9, 0.999, -1.0, 0.0, 1),      # eps < 0
+                AdamHParams(1e-3, 0.9, 0.999, 1e-8, 0.01, 1)):    # weight decay
+        assert step(fake, fake, 0, fake, fake, fake, fake, 10, ctypes.byref(bad), None) == 1
+    assert step(None, fake, 0, fake, fake, fake, fake, 10, ctypes.byref(hp), None) == 1
+
+    multi = lib.bwd_adam8bit_step_multi
+    assert multi(0, None, None, 0, None, None, None, None, None, ctypes.byref(hp), None) == 0
+    assert multi(-1, None, None, 0, None, None, None, None, None, ctypes.byref(hp), None) == 1
+    assert multi(2, None, None, 0, None, None, None, None, None, ctypes.byref(hp), None) == 1
+    arr = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    nul = (ctypes.c_void_p * 2)(0x1000, None)
+    ns = (ctypes.c_int64 * 2)(5, 7)
+    neg = (ctypes.c_int64 * 2)(5, -7)
+    assert multi(2, arr, arr, 0, arr, arr, arr, arr, neg, ctypes.byref(hp), None) == 1
+    assert multi(2, arr, nul, 0, arr, arr, arr, arr, ns, ctypes.byref(hp), None) == 1
+    assert b"tensor 1" in lib.bwd_last_error()

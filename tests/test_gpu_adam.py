@@ -1,0 +1,271 @@
+"""GPU parity: the fused 8-bit Adam step through the C ABI against the
+oracle's step (sections 一 and 二 of "8-BIT OPTIMIZERS VIA BLOCK-WISE
+QUANTIZATION").
+
+Tolerance of a step taken from identical input state: parameters rtol 1e-5,
+atol 1e-7; at most 1e-4 of the codes may differ, each by at most one index;
+absmax rtol 1e-6.  The kernel performs the same binary32 operations in the
+same order as the oracle, so in practice every output is bit-identical; the
+tests also record that exactness."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.adam import widen_bf16
+from block_wise_dynamic_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+B = 2048
+U32 = np.uint32
+
+
+@pytest.fixture(scope="module")
+def bwd():
+    from block_wise_dynamic_gb300 import build
+
+    build.build()
+    import block_wise_dynamic_gb300 as m
+
+    m.init(0)
+    return m
+
+
+def g_to_np(g: torch.Tensor) -> np.ndarray:
+    g = g.detach().cpu()
+    if g.dtype == torch.bfloat16:
+        return widen_bf16(g.view(torch.int16).numpy().view(np.uint16))
+    return g.numpy()
+
+
+def compare_step(gpu, ref, exact=True):
+    """gpu, ref: (p, mc, ma, vc, va) numpy tuples of one tensor."""
+    p, mc, ma, vc, va = gpu
+    rp, rmc, rma, rvc, rva = ref
+    np.testing.assert_allclose(p, rp, rtol=1e-5, atol=1e-7)
+    for c, rc in ((mc, rmc), (vc, rvc)):
+        d = np.abs(c.astype(np.int32) - rc.astype(np.int32))
+        assert d.max(initial=0) <= 1
+        assert np.count_nonzero(d) <= max(1e-4 * c.size, 0)
+    np.testing.assert_allclose(ma, rma, rtol=1e-6, atol=0)
+    np.testing.assert_allclose(va, rva, rtol=1e-6, atol=0)
+    if exact:
+        assert np.array_equal(p.view(U32), rp.view(U32))
+        assert np.array_equal(mc, rmc) and np.array_equal(vc, rvc)
+        assert np.array_equal(ma.view(U32), rma.view(U32)) and np.array_equal(va.view(U32), rva.view(U32))
+
+
+def random_state(n, seed, m_scale=1e-3, v_scale=1e-6):
+    """A non-trivial 8-bit state: random moments quantized by the oracle."""
+    rng = np.random.default_rng(seed)
+    m = (rng.standard_normal(n) * m_scale * 10.0 ** rng.uniform(-2, 0, n)).astype(np.float32)
+    v = (rng.standard_normal(n) ** 2 * v_scale * 10.0 ** rng.uniform(-3, 0, n)).astype(np.float32)
+    mc, ma = oracle.quantize_blockwise(m, True)
+    vc, va = oracle.quantize_blockwise(v, False)
+    return mc, ma, vc, va
+
+
+def to_dev(*arrs):
+    return [torch.from_numpy(np.ascontiguousarray(a)).to(DEV) for a in arrs]
+
+
+def run_gpu(bwd, p, g, st, hp: oracle.AdamHParams):
+    tp, tmc, tma, tvc, tva = to_dev(p, *st)
+    tg = g.to(DEV)
+    bwd.adam8bit_step(tp, tg, tmc, tma, tvc, tva, lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2,
+                      eps=hp.eps, step=hp.step)
+    torch.cuda.synchronize()
+    return tuple(t.cpu().numpy() for t in (tp, tmc, tma, tvc, tva))
+
+
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("n", [1, 2047, 2048, 2049, 5 * B + 77, 1 << 20])
+def test_single_step_from_identical_state(bwd, n, gdt):
+    p = W.gen_normal(n, 0.02, seed=n).numpy()
+    g = W.gen_normal(n, 1e-2, seed=n + 1, dtype=gdt)
+    st = random_state(n, n + 2)
+    for t in (1, 7):
+        hp = oracle.AdamHParams(lr=1e-3, step=t)
+        got = run_gpu(bwd, p, g, st, hp)
+        ref = oracle.adam8bit_step(p, g_to_np(g), *st, hp)
+        compare_step(got, ref)
+
+
+def test_first_step_from_state_init(bwd):
+    n = 3 * B + 5
+    mc, ma, vc, va = bwd.state_init(n, DEV)
+    smc, sma, svc, sva = oracle.state_init(n)
+    assert np.array_equal(mc.cpu().numpy(), smc) and np.array_equal(vc.cpu().numpy(), svc)
+    assert np.all(ma.cpu().numpy() == 0) and np.all(va.cpu().numpy() == 0)
+    p = W.gen_normal(n, 0.02, 1).numpy()
+    g = W.gen_normal(n, 1e-2, 2)
+    got = run_gpu(bwd, p, g, (smc, sma, svc, sva), oracle.AdamHParams(step=1))
+    ref = oracle.adam8bit_step(p, g_to_np(g), smc, sma, svc, sva, oracle.AdamHParams(step=1))
+    compare_step(got, ref)
+
+
+def test_ten_step_trajectory_1m(bwd):
+    """The 1,048,576-element workload for 10 steps with fresh gradients each
+    step, GPU and oracle each carrying their own state."""
+    wl = W.workload("adam_1m")
+    n = wl.sizes[0]
+    p0 = W.gen_normal(n, 0.02, seed=0)
+    tp = p0.to(DEV)
+    mc, ma, vc, va = bwd.state_init(n, DEV)
+    rp = p0.numpy().copy()
+    rst = oracle.state_init(n)
+    for t in range(1, wl.steps + 1):
+        g = W.gen_normal(n, wl.grad_std[0], seed=1000 + t)
+        bwd.adam8bit_step(tp, g.to(DEV), mc, ma, vc, va, lr=wl.lr, step=t)
+        hp = oracle.AdamHParams(lr=wl.lr, step=t)
+        rp, *rst = oracle.adam8bit_step(rp, g.numpy(), *rst, hp)
+    torch.cuda.synchronize()
+    got = (tp.cpu().numpy(), mc.cpu().numpy(), ma.cpu().numpy(), vc.cpu().numpy(), va.cpu().numpy())
+    compare_step(got, (rp, *rst))
+
+
+def _multi_case(bwd, sizes, gdt, seed, offsets=None):
+    """Run one multi-tensor step on the GPU and the oracle per tensor."""
+    rng = np.random.default_rng(seed)
+    host = []
+    dev = []
+    for i, n in enumerate(sizes):
+        off = 0 if offsets is None else offsets[i]
+        p = W.gen_normal(n, 0.02, seed * 7919 + i).numpy()
+        g = W.gen_normal(n, float(10.0 ** rng.uniform(-5, -1)), seed * 7919 + 5000 + i, dtype=gdt)
+        st = random_state(n, seed * 31 + i) if n else oracle.state_init(0)
+        host.append((p, g_to_np(g), *st))
+        # optional element offset makes the buffers unaligned
+        tp = torch.empty(n + off, dtype=torch.float32, device=DEV)[off:]
+        tp.copy_(torch.from_numpy(p))
+        tg = torch.empty(n + off, dtype=gdt, device=DEV)[off:]
+        tg.copy_(g)
+        tmc = torch.empty(n + off, dtype=torch.uint8, device=DEV)[off:]
+        tmc.copy_(torch.from_numpy(st[0]))
+        tvc = torch.empty(n + off, dtype=torch.uint8, device=DEV)[off:]
+        tvc.copy_(torch.from_numpy(st[2]))
+        tma, tva = to_dev(st[1], st[3])
+        dev.append((tp, tg, tmc, tma, tvc, tva))
+    hp = oracle.AdamHParams(lr=2e-3, beta1=0.9, beta2=0.99, eps=1e-8, step=3)
+    lists = list(zip(*dev))
+    bwd.adam8bit_step_multi(*lists, lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps, step=hp.step)
+    torch.cuda.synchronize()
+    for h, d in zip(host, dev):
+        ref = oracle.adam8bit_step(*h, hp)
+        got = tuple(x.cpu().numpy() for x in (d[0], d[2], d[3], d[4], d[5]))
+        compare_step(got, ref)
+
+
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
+def test_multi_ragged_list(bwd, gdt):
+    rng = np.random.default_rng(5)
+    sizes = [int(s) for s in rng.integers(1, 40_000, 60)] + [0, 2048, 4096, 1, 0, 2049]
+    _multi_case(bwd, sizes, gdt, seed=11)
+
+
+def test_multi_more_tensors_than_one_launch_holds(bwd):
+    rng = np.random.default_rng(6)
+    sizes = [int(s) for s in rng.integers(1, 3000, 1000)]
+    _multi_case(bwd, sizes, torch.float32, seed=12)
+
+
+def test_multi_with_unaligned_tensors(bwd):
+    sizes = [2048 * 3, 5000, 2048, 7777]
+    _multi_case(bwd, sizes, torch.bfloat16, seed=13, offsets=[1, 0, 3, 2])
+
+
+def test_optimizer_drop_in_and_exact_resume(bwd):
+    """Adam8bit replaces torch.optim.Adam; saving its state after k steps and
+    resuming reproduces the uninterrupted run bit for bit."""
+    torch.manual_seed(0)
+    model = torch.nn.Sequential(torch.nn.Linear(64, 300), torch.nn.ReLU(), torch.nn.Linear(300, 10)).to(DEV)
+    ref_model = [p.detach().cpu().numpy().ravel().copy() for p in model.parameters()]
+    opt = bwd.Adam8bit(model.parameters(), lr=1e-3)
+    ref_state = [oracle.state_init(p.size) for p in ref_model]
+    x = torch.randn(128, 64, device=DEV)
+    y = torch.randint(0, 10, (128,), device=DEV)
+    saved = None
+    for t in range(1, 7):
+        opt.zero_grad()
+        loss = torch.nn.functional.cross_entropy(model(x), y)
+        loss.backward()
+        grads = [p.grad.detach().cpu().numpy().ravel() for p in model.parameters()]
+        opt.step()
+        hp = oracle.AdamHParams(lr=1e-3, step=t)
+        for i, g in enumerate(grads):
+            ref_model[i], *ref_state[i] = oracle.adam8bit_step(ref_model[i], g, *ref_state[i], hp)
+        for i, p in enumerate(model.parameters()):
+            st = opt.state[p]
+            got = (p.detach().cpu().numpy().ravel(), st["m_codes"].cpu().numpy(), st["m_absmax"].cpu().numpy(),
+                   st["v_codes"].cpu().numpy(), st["v_absmax"].cpu().numpy())
+            compare_step(got, (ref_model[i], *ref_state[i]))
+        if t == 3:
+            saved = ({k: v.clone() for k, v in model.state_dict().items()},
+                     {"state": {k: {kk: (vv.clone() if torch.is_tensor(vv) else vv) for kk, vv in s.items()}
+                                for k, s in opt.state_dict()["state"].items()},
+                      "param_groups": opt.state_dict()["param_groups"]})
+    final = [p.detach().clone() for p in model.parameters()]
+    # resume from step 3
+    model.load_state_dict(saved[0])
+    opt2 = bwd.Adam8bit(model.parameters(), lr=1e-3)
+    opt2.load_state_dict(saved[1])
+    for p in model.parameters():
+        assert opt2.state[p]["m_codes"].dtype == torch.uint8
+    for t in range(4, 7):
+        opt2.zero_grad()
+        torch.nn.functional.cross_entropy(model(x), y).backward()
+        opt2.step()
+    for a, b in zip(final, model.parameters()):
+        assert torch.equal(a, b.detach())
+
+
+def _sampled_full_size(bwd, wl, blocks_per_tensor=2, max_tensors=80, steps=2, seed=0):
+    """Run the whole workload through one multi-tensor call per step (the
+    launch configuration the bench times) and check sampled blocks of the
+    last step against the oracle, from the GPU's own input state."""
+    rng = np.random.default_rng(seed)
+    T = len(wl.sizes)
+    ps, gs, sts = [], [], []
+    for i, n in enumerate(wl.sizes):
+        ps.append(W.gen_normal(n, 0.02, seed=i, device=DEV))
+        gs.append(W.gen_normal(n, wl.grad_std[i], seed=100_000 + i, device=DEV, dtype=wl.grad_dtype))
+        sts.append(bwd.state_init(n, DEV))
+    args = bwd.MultiTensorArgs(ps, gs, *[[s[k] for s in sts] for k in range(4)])
+    for t in range(1, steps):
+        args.step(lr=wl.lr, step=t)
+    pick = sorted(set([0, T - 1]) | set(rng.choice(T, min(T, max_tensors), replace=False).tolist()))
+    samples = []
+    for i in pick:
+        n = wl.sizes[i]
+        nb = (n + B - 1) // B
+        for b in sorted(set([0, nb - 1]) | set(rng.choice(nb, min(nb, blocks_per_tensor), replace=False).tolist())):
+            lo, hi = b * B, min(n, (b + 1) * B)
+            inp = (ps[i][lo:hi].cpu().numpy(), g_to_np(gs[i][lo:hi]), sts[i][0][lo:hi].cpu().numpy(),
+                   sts[i][1][b:b + 1].cpu().numpy(), sts[i][2][lo:hi].cpu().numpy(),
+                   sts[i][3][b:b + 1].cpu().numpy())
+            samples.append((i, b, lo, hi, inp))
+    args.step(lr=wl.lr, step=steps)
+    torch.cuda.synchronize()
+    hp = oracle.AdamHParams(lr=wl.lr, step=steps)
+    for i, b, lo, hi, inp in samples:
+        ref = oracle.adam8bit_step(*inp, hp)
+        got = (ps[i][lo:hi].cpu().numpy(), sts[i][0][lo:hi].cpu().numpy(), sts[i][1][b:b + 1].cpu().numpy(),
+               sts[i][2][lo:hi].cpu().numpy(), sts[i][3][b:b + 1].cpu().numpy())
+        compare_step(got, ref)
+    del ps, gs, sts, args
+    torch.cuda.empty_cache()
+    return len(samples)
+
+
+def test_full_size_llama2_7b_sampled(bwd):
+    assert _sampled_full_size(bwd, W.workload("llama2_7b")) > 100
+
+
+def test_full_size_ragged_2000_sampled(bwd):
+    assert _sampled_full_size(bwd, W.workload("ragged_2000")) > 100
+
+
+def test_full_size_gpt_350m_flat_sampled(bwd):
+    assert _sampled_full_size(bwd, W.workload("gpt_350m"), blocks_per_tensor=200) > 100

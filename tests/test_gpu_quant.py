@@ -1,0 +1,168 @@
+"""GPU parity: block-wise quantize / dequantize through the C ABI, bit-exact
+against the oracle (section 二 / 逐块量化 and 动态量化 of "8-BIT OPTIMIZERS VIA
+BLOCK-WISE QUANTIZATION")."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_wise_dynamic_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+U32 = np.uint32
+
+
+@pytest.fixture(scope="module")
+def bwd():
+    from block_wise_dynamic_gb300 import build
+
+    build.build()
+    import block_wise_dynamic_gb300 as m
+
+    m.init(0)
+    return m
+
+
+def kind(signed):
+    return "signed" if signed else "unsigned"
+
+
+def gpu_quant(bwd, x_np, signed):
+    x = torch.from_numpy(np.ascontiguousarray(x_np, np.float32)).to(DEV)
+    c, a = bwd.quantize_blockwise(x, kind(signed))
+    return c.cpu().numpy(), a.cpu().numpy()
+
+
+def gpu_dequant(bwd, c_np, a_np, signed):
+    c = torch.from_numpy(c_np).to(DEV)
+    a = torch.from_numpy(a_np).to(DEV)
+    return bwd.dequantize_blockwise(c, a, kind(signed)).cpu().numpy()
+
+
+SIZES = [1, 2, 31, 2047, 2048, 2049, 4095, 4096, 3 * 2048 + 17, (1 << 20) + 123]
+
+
+@pytest.mark.parametrize("signed", [True, False])
+@pytest.mark.parametrize("n", SIZES)
+def test_quantize_dequantize_bit_exact(bwd, n, signed):
+    x = W.quant_input(n, seed=n).numpy()
+    if not signed:
+        x = x * x
+    c, a = gpu_quant(bwd, x, signed)
+    co, ao = oracle.quantize_blockwise(x, signed)
+    assert np.array_equal(a.view(U32), ao.view(U32))
+    assert np.array_equal(c, co)
+    y = gpu_dequant(bwd, co, ao, signed)
+    yo = oracle.dequantize_blockwise(co, ao, signed)
+    assert np.array_equal(y.view(U32), yo.view(U32))
+
+
+@pytest.mark.parametrize("signed", [True, False])
+def test_unaligned_buffers_take_the_elementwise_path(bwd, signed):
+    n = 5 * 2048 + 300
+    x = W.quant_input(n + 1, seed=9).to(DEV)
+    if not signed:
+        x = x * x
+    xv = x[1:]  # 4-byte offset: not 16-byte aligned
+    codes = torch.empty(n + 3, dtype=torch.uint8, device=DEV)[3:]
+    absmax = torch.empty((n + 2047) // 2048, dtype=torch.float32, device=DEV)
+    bwd.quantize_blockwise(xv, kind(signed), codes=codes, absmax=absmax)
+    co, ao = oracle.quantize_blockwise(xv.cpu().numpy(), signed)
+    assert np.array_equal(codes.cpu().numpy(), co)
+    assert np.array_equal(absmax.cpu().numpy().view(U32), ao.view(U32))
+    out = torch.empty(n + 1, dtype=torch.float32, device=DEV)[1:]
+    bwd.dequantize_blockwise(codes, absmax, kind(signed), out=out)
+    yo = oracle.dequantize_blockwise(co, ao, signed)
+    assert np.array_equal(out.cpu().numpy().view(U32), yo.view(U32))
+
+
+@pytest.mark.parametrize("signed", [True, False])
+def test_zero_blocks_and_signed_zeros(bwd, signed):
+    B = 2048
+    x = np.zeros(4 * B + 5, np.float32)
+    x[B:2 * B] = -0.0
+    x[2 * B:3 * B] = np.linspace(-1, 1, B, dtype=np.float32) if signed else np.linspace(0, 1, B, dtype=np.float32)
+    x[2 * B + 7] = -0.0
+    x[2 * B + 9] = 0.0
+    x[3 * B + 1] = -1e-30 if signed else 1e-30
+    c, a = gpu_quant(bwd, x, signed)
+    co, ao = oracle.quantize_blockwise(x, signed)
+    assert np.array_equal(c, co) and np.array_equal(a.view(U32), ao.view(U32))
+    z = 128 if signed else 0
+    assert np.all(c[:2 * B] == z) and a[0] == 0 and a[1] == 0
+    y = gpu_dequant(bwd, c, a, signed)
+    assert np.array_equal(y.view(U32), oracle.dequantize_blockwise(co, ao, signed).view(U32))
+
+
+def _bits_range(lo_bits, hi_bits):
+    return np.arange(lo_bits, hi_bits + 1, dtype=np.uint32).view(np.float32)
+
+
+def _normalised_sweep(signed):
+    """Normalised values that stress the code decision: every value of
+    [0.5, 1]; +-64 ulps around every threshold; +-2 ulps around every 2^-16
+    of the binary32 pattern range (the bucket edges of the lookup); a stride
+    through all of (0, 1]; and tiny values."""
+    t = oracle.thresholds(signed)
+    parts = [_bits_range(0x3F000000, 0x3F800000)]
+    tb = np.abs(t[t != 0]).view(U32).astype(np.int64)
+    offs = np.arange(-64, 65)
+    parts.append((tb[:, None] + offs[None, :]).ravel().astype(U32).view(np.float32))
+    edges = (np.arange((127 - 27) << 7, (127 << 7) + 1, dtype=np.int64) << 16)
+    parts.append((edges[:, None] + np.arange(-2, 3)[None, :]).ravel().astype(U32).view(np.float32))
+    parts.append(_bits_range(1, 0x3F800000)[::97])
+    parts.append(np.array([0.0, 1e-45, 1e-38, 1e-30, 4.9999997e-8, 5e-8, 5.0000004e-8], np.float32))
+    v = np.unique(np.concatenate(parts))
+    v = v[(v >= 0) & (v <= 1)]
+    if signed:
+        v = np.concatenate([v, -v])
+    return v.astype(np.float32)
+
+
+@pytest.mark.parametrize("signed", [True, False])
+def test_code_decision_sweep(bwd, signed):
+    """Blocks lead with 1.0, so absmax = 1 and x / absmax = x: the codes of
+    the swept values must equal the oracle's."""
+    v = _normalised_sweep(signed)
+    per = 2047
+    nb = (v.size + per - 1) // per
+    pad = np.zeros(nb * per, np.float32)
+    pad[: v.size] = v
+    rows = np.concatenate([np.ones((nb, 1), np.float32), pad.reshape(nb, per)], axis=1).ravel()
+    c, a = gpu_quant(bwd, rows, signed)
+    co, ao = oracle.quantize_blockwise(rows, signed)
+    assert np.all(a == 1.0)
+    bad = np.nonzero(c != co)[0]
+    assert bad.size == 0, f"{bad.size} codes differ, first at value {rows[bad[0]]!r}"
+
+
+def test_full_size_2p28_sampled(bwd):
+    """The 2^28-element workload: absmax of every block checked against a
+    plain max, codes and dequantized values of sampled blocks bit-exact."""
+    n = 1 << 28
+    B = 2048
+    x = W.quant_input(n, seed=0, device=DEV)
+    rng = np.random.default_rng(0)
+    nb = n // B
+    out_blocks = np.unique((np.nonzero((x.abs() > 20).view(-1, B).any(1).cpu().numpy())[0]))
+    sample = np.unique(np.concatenate([[0, nb - 1], rng.choice(nb, 96, replace=False), out_blocks[:32]]))
+    for signed in (True, False):
+        xs = x if signed else x * x
+        c, a = bwd.quantize_blockwise(xs, kind(signed))
+        torch.cuda.synchronize()
+        ref_absmax = xs.view(-1, B).abs().amax(dim=1)
+        assert torch.equal(a, ref_absmax)
+        y = bwd.dequantize_blockwise(c, a, kind(signed))
+        xc = xs.view(-1, B)[sample].cpu().numpy()
+        cc = c.view(-1, B)[sample].cpu().numpy()
+        yc = y.view(-1, B)[sample].cpu().numpy()
+        for r in range(len(sample)):
+            co, ao = oracle.quantize_blockwise(xc[r], signed)
+            assert np.array_equal(cc[r], co)
+            yo = oracle.dequantize_blockwise(co, ao, signed)
+            assert np.array_equal(yc[r].view(U32), yo.view(U32))
+        del c, a, y, xs
+    del x
+    torch.cuda.empty_cache()
