@@ -48,7 +48,8 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="llama2_7b", choices=["llama2_7b", "gpt_350m", "ragged_2000", "adam_1m"])
+    ap.add_argument("--workload", default="llama2_7b",
+                    choices=["llama2_7b", "gpt_350m", "ragged_2000", "adam_1m", "quant_2p28"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -207,18 +208,26 @@ def run_reference(args):
     world, rank, _ = dist_info()
     if rank != 0:
         return
-    n = 1024 * 2048
-    rate, dt = oracle_rate(n, steps=args.steps, warm=args.warmup)
+    if args.workload == "quant_2p28":
+        n = 2 ** 20
+        if args.warmup:
+            oracle_quant_rate(n, steps=args.warmup)
+        rate, dt = oracle_quant_rate(n, steps=args.steps)
+        unit, what = "elements/s", f"each step: the oracle's four passes on {n} elements, single process"
+    else:
+        n = 1024 * 2048
+        rate, dt = oracle_rate(n, steps=args.steps, warm=args.warmup)
+        unit = "params/s"
+        what = (f"each step: the oracle's 8-bit Adam step on {n} params (1024 blocks) "
+                f"of the {args.workload} distributions, single process")
     line = {
-        "impl": "reference", "metric": METRIC, "value": rate, "unit": "params/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": args.workload, "sample_params_per_step": n},
-        "cpu_baseline": {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
-                         "sample": f"each step: the oracle's 8-bit Adam step on {n} params (1024 blocks) "
-                                   f"of the {args.workload} distributions, single process"},
-        "e2e": {"value": rate, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": rate, "unit": unit, "cores": 1, "kind": "oracle", "sample": what},
+        "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -395,10 +404,157 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+QUANT_BYTES_PER_ELEM = 4 + 1 + 4.0 / 2048  # fp32 in or out, one code, absmax per block
+
+
+def oracle_quant_rate(n: int, steps: int):
+    """Elements/s of the oracle's four passes (quantize + dequantize with the
+    signed map on x, the unsigned map on x^2) over a sample of n elements."""
+    import oracle
+    from block_wise_dynamic_gb300 import workloads as W
+
+    x = W.quant_input(n, seed=0).numpy()
+    x2 = x * x
+    oracle.quantize_blockwise(x[:2048], True)
+    oracle.quantize_blockwise(x[:2048], False)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        c, a = oracle.quantize_blockwise(x, True)
+        oracle.dequantize_blockwise(c, a, True)
+        c, a = oracle.quantize_blockwise(x2, False)
+        oracle.dequantize_blockwise(c, a, False)
+    dt = time.perf_counter() - t0
+    return 4 * n * steps / dt, dt
+
+
+def run_quant(args):
+    """The standalone 2^28-element quantize / dequantize workload."""
+    import torch
+
+    import block_wise_dynamic_gb300 as bwd
+    from block_wise_dynamic_gb300 import workloads as W
+
+    world, rank, local = dist_info()
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    bwd.init(dev)
+    n = 1 << 28
+    x = W.quant_input(n, seed=rank, device=dev)
+    x2 = x * x
+    codes = torch.empty(n, dtype=torch.uint8, device=dev)
+    absmax = torch.empty(bwd.num_blocks(n), dtype=torch.float32, device=dev)
+    y = torch.empty(n, dtype=torch.float32, device=dev)
+    passes = [
+        ("quantize_signed", lambda: bwd.quantize_blockwise(x, "signed", codes, absmax)),
+        ("dequantize_signed", lambda: bwd.dequantize_blockwise(codes, absmax, "signed", out=y)),
+        ("quantize_unsigned", lambda: bwd.quantize_blockwise(x2, "unsigned", codes, absmax)),
+        ("dequantize_unsigned", lambda: bwd.dequantize_blockwise(codes, absmax, "unsigned", out=y)),
+    ]
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        for _, f in passes:
+            f()
+    torch.cuda.synchronize(dev)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in passes]
+          for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    c0 = time.perf_counter()
+    e0.record(stream)
+    for k in range(args.steps):
+        for j, (_, f) in enumerate(passes):
+            ev[k][j][0].record(stream)
+            f()
+            ev[k][j][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    c1 = time.perf_counter()
+    clocks.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    per_pass = {}
+    for j, (name, _) in enumerate(passes):
+        ms = statistics.fmean(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(args.steps))
+        per_pass[name] = {"ms": ms, "elems_per_s": n / (ms / 1e3),
+                          "gbs": QUANT_BYTES_PER_ELEM * n / (ms / 1e3) / 1e9}
+
+    # end to end: x and x^2 from pinned host memory, both dequantized outputs back
+    e2e = None
+    if args.e2e_steps > 0:
+        xh = torch.empty(n, dtype=torch.float32, pin_memory=True)
+        x2h = torch.empty(n, dtype=torch.float32, pin_memory=True)
+        yh = torch.empty(2, n, dtype=torch.float32, pin_memory=True)
+        xh.copy_(x)
+        x2h.copy_(x2)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        f0.record(stream)
+        for _ in range(args.e2e_steps):
+            x.copy_(xh, non_blocking=True)
+            x2.copy_(x2h, non_blocking=True)
+            for j, (_, f) in enumerate(passes):
+                f()
+                if j % 2 == 1:
+                    yh[j // 2].copy_(y, non_blocking=True)
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e = {"value": world * 4 * n * args.e2e_steps / (f0.elapsed_time(f1) / 1e3), "unit": "elements/s",
+               "h2d_bytes_per_step": 8 * n, "d2h_bytes_per_step": 8 * n, "steps": args.e2e_steps,
+               "what": "per step: H2D of x and x^2 from pinned host memory, the four passes, D2H of both "
+                       "dequantized outputs into pinned host memory, one stream"}
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    dom = max(per_pass, key=lambda k: per_pass[k]["ms"])
+    peak, peak_kind = measured_peak()
+    achieved = per_pass[dom]["gbs"]
+    line = {
+        "metric": METRIC, "value": world * 4 * n * args.steps / (elapsed_ms / 1e3), "unit": "elements/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "quant_2p28", "elements": n,
+                   "step": "quantize(x, signed), dequantize, quantize(x^2, unsigned), dequantize",
+                   "l2": "inputs larger than L2 (1 GiB fp32 per pass vs 126 MiB L2), no flush",
+                   "parallelism": f"replica per GPU x{world}"},
+        "passes": per_pass,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} (copy bandwidth)", "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "bytes_per_elem": QUANT_BYTES_PER_ELEM,
+                     "mean_launch_ms": per_pass[dom]["ms"]},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks.summary(c0, c1),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        m = 4 * 2 ** 20
+        rate, dt = oracle_quant_rate(m, steps=2)
+        line["cpu_baseline"] = {"value": rate, "unit": "elements/s", "cores": 1, "kind": "oracle",
+                                "sample": f"2 steps of the four oracle passes on {m} elements, {dt:.1f} s, "
+                                          "single process"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "quant_2p28":
+        run_quant(args)
     else:
         run_ours(args)
 

@@ -77,22 +77,31 @@ float from_bits(uint32_t u) {
   return f;
 }
 
-int build_buckets(const float* t, uint8_t* bkt, char* err, size_t errlen) {
-  for (int b = 0; b < kBktPad; ++b) bkt[b] = 0;
-  for (int b = 0; b < kNumBkt; ++b) {
-    const uint32_t lo_bits = b == 0 ? 0u : static_cast<uint32_t>(kBktBase + b) << kBktShift;
-    const float lo = from_bits(lo_bits);
-    int c = 0;
-    while (c < kCodes - 1 && t[c] <= lo) ++c;
-    bkt[b] = static_cast<uint8_t>(c);
-    if (b + 1 < kNumBkt && c + 1 < kCodes - 1) {
-      // largest value of the bucket: one below the next bucket's first
-      const float hi = from_bits((static_cast<uint32_t>(kBktBase + b + 1) << kBktShift) - 1u);
-      if (!(t[c + 1] > hi)) {
-        std::snprintf(err, errlen, "bucket %d holds two thresholds", b);
-        return -1;
-      }
-    }
+// One bucket: values from v_lo to v_hi (v_lo <= v_hi).  Stores the count of
+// thresholds <= v_lo and checks that (v_lo, v_hi] holds at most one more.
+int fill_bucket(const float* t, float v_lo, float v_hi, uint8_t* out, char* err, size_t errlen) {
+  int c = 0;
+  while (c < kCodes - 1 && t[c] <= v_lo) ++c;
+  *out = static_cast<uint8_t>(c);
+  if (c + 1 < kCodes - 1 && !(t[c + 1] > v_hi)) {
+    std::snprintf(err, errlen, "bucket [%a, %a] holds two thresholds", v_lo, v_hi);
+    return -1;
+  }
+  return 0;
+}
+
+int build_counts(const float* ts, const float* tu, uint8_t* cnt, char* err, size_t errlen) {
+  std::memset(cnt, 255, kCntPad);
+  for (uint32_t i = 0; i <= kCntUnsignedMax; ++i) {
+    // non-negative patterns: the lowest value has the smallest pattern
+    const float lo = from_bits(i << 16), hi = from_bits((i << 16) | 0xffffu);
+    if (fill_bucket(ts, lo, hi, &cnt[i], err, errlen) != 0) return -1;
+    if (fill_bucket(tu, lo, hi, &cnt[i + kCntUnsignedOff], err, errlen) != 0) return -1;
+  }
+  for (uint32_t i = 0x8000u; i <= kCntSignedMax; ++i) {
+    // negative patterns: the lowest value has the largest pattern
+    const float lo = from_bits((i << 16) | 0xffffu), hi = from_bits(i << 16);
+    if (fill_bucket(ts, lo, hi, &cnt[i], err, errlen) != 0) return -1;
   }
   return 0;
 }
@@ -103,9 +112,8 @@ int build_tables(Tables* tab, char* err, size_t errlen) {
   for (int k = 0; k < 2; ++k) {
     build_map(k == 0, tab->map[k]);
     build_thresholds(tab->map[k], tab->thr[k]);
-    if (build_buckets(tab->thr[k], tab->bkt[k], err, errlen) != 0) return -1;
   }
-  return 0;
+  return build_counts(tab->thr[0], tab->thr[1], tab->cnt, err, errlen);
 }
 
 }  // namespace bwd

@@ -8,16 +8,23 @@
 // optimizer dequantizes its states, updates in high precision (fp32) and
 // stores them quantized again.
 //
-// Work decomposition.  One CTA of 256 threads owns one 2048-element block at
-// a time and walks blocks with a grid stride (grid = SMs x resident CTAs).
-// Thread `tid` owns elements {4 tid .. 4 tid + 3} and {1024 + 4 tid .. +3} of
-// the block, so every warp-wide load or store touches one contiguous span
-// (512 B of fp32, 256 B of bf16, 128 B of codes) and is fully coalesced.  The
-// block absmax is a warp shuffle reduction followed by a shared-memory pass
-// over the 8 warps.  The map, thresholds and bucket tables live in shared
-// memory.  All arithmetic that decides a code (absmax, x / absmax, the
-// threshold compare) is plain IEEE binary32, with explicit round-to-nearest
-// intrinsics so that no multiply-add is ever contracted.
+// Work decomposition.  A group of 128 threads owns one 2048-element block at a
+// time; a CTA holds two groups and the groups walk the blocks with a grid
+// stride (grid = SMs x resident CTAs).  Thread t of a group owns the 16
+// elements 4 t + 512 k + j (k, j < 4) of its block, so every warp-wide load or
+// store touches one contiguous span (512 B of fp32, 256 B of bf16, 128 B of
+// codes) and is fully coalesced.  The block absmax is a warp shuffle
+// reduction and a pass over the group's four warps through shared memory,
+// synchronised by a named barrier per group.  The maps, thresholds and the
+// count table (tables.h) are copied once per CTA into dynamic shared memory.
+//
+// Exactness.  Every operation that decides a code is IEEE binary32 with
+// explicit round-to-nearest intrinsics (no contracted multiply-add): the
+// absmax, the quotient x / absmax (exact_div.cuh gives the correctly rounded
+// quotient from a per-block reciprocal; tiny negative quotients, where -0.0
+// and a negative subnormal give different codes, fall back to div.rn) and
+// the threshold compare.  The Adam update uses the same operations, in the
+// same order, as the CPU oracle.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -28,19 +35,24 @@
 #include <string>
 
 #include "bwd.h"
+#include "exact_div.cuh"
 #include "tables.h"
 
 namespace {
 
-using bwd::kBktBase;
-using bwd::kBktPad;
 using bwd::kCodes;
-using bwd::kNumBkt;
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kMaxTensors = 448;  // per launch, bounded by kernel parameter space
+constexpr int kGroup = 128;                   // threads per 2048-element block
+constexpr int kPer = BWD_BLOCK / kGroup;      // 16 elements per thread
+constexpr int kGroupWarps = kGroup / 32;      // 4
+constexpr int kGroups = 2;                    // blocks in flight per CTA
+constexpr int kCta = kGroup * kGroups;        // 256 threads
+constexpr int kDeqThreads = 256;              // dequantize: 8 elements per thread
+constexpr int kMaxTensors = 448;              // per launch, bounded by kernel parameter space
 constexpr int kMaxDevices = 64;
+constexpr int kTablesBytes = static_cast<int>(sizeof(bwd::Tables));
+
+static_assert(kPer == 16, "the element layout below assumes 16 elements per thread");
 
 __device__ bwd::Tables g_tables;  // immutable after the first upload per device
 
@@ -53,51 +65,23 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Number of thresholds <= y for y >= +0 given as its bit pattern (see the
-// bucket table description in tables.h).  Indices are clamped, so any input
-// pattern stays inside the tables.
-__device__ __forceinline__ uint32_t count_le(uint32_t ybits, const uint8_t* bkt, const float* thr) {
-  int b = static_cast<int>(ybits >> bwd::kBktShift) - kBktBase;
-  b = min(max(b, 0), kNumBkt - 1);
-  const uint32_t c = bkt[b];
-  return c + (thr[c] <= __uint_as_float(ybits) ? 1u : 0u);
+// Named barrier of one 128-thread group (barrier 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "n"(kGroup) : "memory");
 }
 
-// Signed map.  For xn >= 0 (including -0.0) the code is count(xn).  The
-// thresholds are antisymmetric, t[254 - i] = -t[i], so for xn = -a < 0 the
-// count of thresholds <= -a is 255 - #{t < a} = 255 - count(pred(a)), where
-// pred(a) is the next binary32 value below a.
-__device__ __forceinline__ uint32_t code_signed(float xn, const uint8_t* bkt, const float* thr) {
-  const uint32_t u = __float_as_uint(xn);
-  const uint32_t a = u & 0x7fffffffu;
-  const bool neg = (u != a) && (a != 0u);
-  const uint32_t c = count_le(neg ? a - 1u : a, bkt, thr);
-  return neg ? 255u - c : c;
-}
+// Element of the block owned by slot j (0..15) of thread t.
+__device__ __forceinline__ int slot(int t, int j) { return 4 * t + 512 * (j >> 2) + (j & 3); }
 
-// Unsigned map: every threshold is positive, so a negative input has code 0.
-__device__ __forceinline__ uint32_t code_unsigned(float xn, const uint8_t* bkt, const float* thr) {
-  const uint32_t u = __float_as_uint(xn);
-  const uint32_t c = count_le(u, bkt, thr);
-  return (u >> 31) ? 0u : c;
-}
-
-template <bool kSigned>
-__device__ __forceinline__ uint32_t quantize_one(float x, float absmax, const uint8_t* bkt,
-                                                 const float* thr) {
-  const float xn = __fdiv_rn(x, absmax);
-  return kSigned ? code_signed(xn, bkt, thr) : code_unsigned(xn, bkt, thr);
-}
-
-// Elements of a block present in a tensor of n elements (1..2048).
 __device__ __forceinline__ int64_t rem_in_block(int64_t n, int64_t base) {
   const int64_t r = n - base;
   return r < BWD_BLOCK ? r : BWD_BLOCK;
 }
 
-// Element slot k (0..7) of thread tid inside a block.
-__device__ __forceinline__ int slot_index(int tid, int k) {
-  return (k < 4) ? 4 * tid + k : 1024 + 4 * tid + (k - 4);
+__device__ __forceinline__ uint32_t byte_of(uint32_t w, int k) { return (w >> (8 * k)) & 0xffu; }
+
+__device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return a | (b << 8) | (c << 16) | (d << 24);
 }
 
 __device__ __forceinline__ void copy_to_smem(void* dst, const void* src, int bytes) {
@@ -106,77 +90,146 @@ __device__ __forceinline__ void copy_to_smem(void* dst, const void* src, int byt
   for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x) d[i] = s[i];
 }
 
-// --------------------------------------------------------------------------
-// quantize
+// Code of a normalised value (see the count table in tables.h).  The clamp
+// keeps any bit pattern, non-finite ones included, inside the table.
+__device__ __forceinline__ uint32_t code_signed(float q, const bwd::Tables& tab) {
+  const uint32_t c = tab.cnt[min(__float_as_uint(q) >> 16, bwd::kCntSignedMax)];
+  return c + (tab.thr[0][c] <= q ? 1u : 0u);
+}
 
-template <bool kSigned>
-__global__ void __launch_bounds__(kThreads)
-quantize_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ codes,
-                float* __restrict__ absmax, int vec_ok) {
-  __shared__ __align__(16) float s_thr[kCodes];
-  __shared__ __align__(16) uint8_t s_bkt[kBktPad];
-  __shared__ float s_red[2][kWarps];
-  const int k = kSigned ? 0 : 1;
-  copy_to_smem(s_thr, g_tables.thr[k], sizeof(s_thr));
-  copy_to_smem(s_bkt, g_tables.bkt[k], sizeof(s_bkt));
-  __syncthreads();
+// Unsigned map, q >= +0 (the second moment is never negative).
+__device__ __forceinline__ uint32_t code_unsigned_nonneg(float q, const bwd::Tables& tab) {
+  const uint32_t c = tab.cnt[min(__float_as_uint(q) >> 16, bwd::kCntUnsignedMax) + bwd::kCntUnsignedOff];
+  return c + (tab.thr[1][c] <= q ? 1u : 0u);
+}
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t nb = (n + BWD_BLOCK - 1) / BWD_BLOCK;
-  const uint32_t zc = kSigned ? 128u : 0u;
-  int it = 0;
-  for (int64_t b = blockIdx.x; b < nb; b += gridDim.x, ++it) {
-    const int64_t base = b * BWD_BLOCK;
-    const int rem = static_cast<int>(rem_in_block(n, base));
-    const bool vec = vec_ok && rem == BWD_BLOCK;
-    float v[8];
-    if (vec) {
-      const float4 a0 = __ldcs(reinterpret_cast<const float4*>(x + base) + tid);
-      const float4 a1 = __ldcs(reinterpret_cast<const float4*>(x + base + 1024) + tid);
-      v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
-      v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+// Unsigned map, any sign: every threshold is positive, so a negative input
+// has code 0.
+__device__ __forceinline__ uint32_t code_unsigned(float q, const bwd::Tables& tab) {
+  const uint32_t c = code_unsigned_nonneg(q, tab);
+  return (__float_as_uint(q) >> 31) ? 0u : c;
+}
+
+// Codes of 16 values of one block with absmax a.  The fast path is straight
+// line (one exact quotient per value from the block's reciprocal, see
+// exact_div.cuh).  Quotients of magnitude below 2^-99 may be off there; only a
+// negative one can change a code (-0.0 -> code 128, a negative subnormal ->
+// code 127), so those are flagged and redone with IEEE division afterwards.
+template <bool kSigned, bool kAnySign>
+__device__ __forceinline__ void quantize16(const float (&x)[kPer], float a, const bwd::Tables& tab,
+                                           uint32_t (&w)[4]) {
+  uint32_t c[kPer];
+  if (a == 0.0f) {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) c[j] = kSigned ? 128u : 0u;
+  } else {
+    const bwd::Divisor d = bwd::make_divisor(a, 1u);
+    if (d.fast) {
+      bool fix = false;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const float q = bwd::div_fast(d, x[j]);
+        if (kSigned) fix |= (x[j] < 0.0f) & (q > -0x1p-99f);
+        c[j] = kSigned ? code_signed(q, tab) : (kAnySign ? code_unsigned(q, tab) : code_unsigned_nonneg(q, tab));
+      }
+      if (kSigned && fix) {
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+          if (x[j] < 0.0f && bwd::div_fast(d, x[j]) > -0x1p-99f) c[j] = code_signed(__fdiv_rn(x[j], a), tab);
+      }
     } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int e = slot_index(tid, j);
-        v[j] = e < rem ? x[base + e] : 0.0f;
+      for (int j = 0; j < kPer; ++j) {
+        const float q = __fdiv_rn(x[j], a);
+        c[j] = kSigned ? code_signed(q, tab) : code_unsigned(q, tab);
       }
     }
-    float mx = 0.0f;
+  }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(v[j]));
-    mx = warp_max(mx);
-    if (lane == 0) s_red[it & 1][warp] = mx;
-    __syncthreads();
-    float am = s_red[it & 1][0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) am = fmaxf(am, s_red[it & 1][w]);
+  for (int k = 0; k < 4; ++k) w[k] = pack4(c[4 * k], c[4 * k + 1], c[4 * k + 2], c[4 * k + 3]);
+}
 
-    uint32_t c[8];
+// Max over the 128 threads of a group; every thread gets the result.
+// `red` is this group's [2 parities][values][4 warps] scratch.
+template <int kVals>
+__device__ __forceinline__ void group_max(float (&v)[kVals], float* red, int parity, int group, int t) {
+  const int lane = t & 31, warp = t >> 5;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      c[j] = (am == 0.0f) ? zc : quantize_one<kSigned>(v[j], am, s_bkt, s_thr);
-    if (vec) {
-      const uint32_t w0 = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-      const uint32_t w1 = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
-      __stcs(reinterpret_cast<unsigned int*>(codes + base) + tid, w0);
-      __stcs(reinterpret_cast<unsigned int*>(codes + base + 1024) + tid, w1);
-    } else {
+  for (int i = 0; i < kVals; ++i) v[i] = warp_max(v[i]);
+  if (lane == 0) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int e = slot_index(tid, j);
-        if (e < rem) codes[base + e] = static_cast<uint8_t>(c[j]);
-      }
-    }
-    if (tid == 0) absmax[b] = am;
+    for (int i = 0; i < kVals; ++i) red[(parity * kVals + i) * kGroupWarps + warp] = v[i];
+  }
+  group_sync(group);
+#pragma unroll
+  for (int i = 0; i < kVals; ++i) {
+    const float4 r = *reinterpret_cast<const float4*>(&red[(parity * kVals + i) * kGroupWarps]);
+    v[i] = fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w));
   }
 }
 
 // --------------------------------------------------------------------------
-// dequantize
+// quantize
 
 template <bool kSigned>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kCta, 4)
+quantize_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ codes,
+                float* __restrict__ absmax, int vec_ok) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  bwd::Tables& tab = *reinterpret_cast<bwd::Tables*>(smem_raw);
+  __shared__ __align__(16) float s_red[kGroups][2 * kGroupWarps];
+  copy_to_smem(&tab, &g_tables, kTablesBytes);
+  __syncthreads();
+
+  const int group = threadIdx.x / kGroup, t = threadIdx.x % kGroup;
+  const int64_t nb = (n + BWD_BLOCK - 1) / BWD_BLOCK;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kGroups;
+  int it = 0;
+  for (int64_t b = static_cast<int64_t>(blockIdx.x) * kGroups + group; b < nb; b += stride, ++it) {
+    const int64_t base = b * BWD_BLOCK;
+    const int rem = static_cast<int>(rem_in_block(n, base));
+    const bool vec = vec_ok && rem == BWD_BLOCK;
+    float v[kPer];
+    if (vec) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(x + base + 512 * k) + t);
+        v[4 * k] = a.x; v[4 * k + 1] = a.y; v[4 * k + 2] = a.z; v[4 * k + 3] = a.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int e = slot(t, j);
+        v[j] = e < rem ? x[base + e] : 0.0f;  // padding leaves max |x| unchanged
+      }
+    }
+    float mx[1] = {0.0f};
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) mx[0] = fmaxf(mx[0], fabsf(v[j]));
+    group_max<1>(mx, s_red[group], it & 1, group, t);
+    const float am = mx[0];
+
+    uint32_t w[4];
+    quantize16<kSigned, true>(v, am, tab, w);
+    if (vec) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) __stcs(reinterpret_cast<unsigned int*>(codes + base + 512 * k) + t, w[k]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int e = slot(t, j);
+        if (e < rem) codes[base + e] = static_cast<uint8_t>(byte_of(w[j >> 2], j & 3));
+      }
+    }
+    if (t == 0) absmax[b] = am;
+  }
+}
+
+// --------------------------------------------------------------------------
+// dequantize (256 threads, 8 elements per thread: 4 t + j and 1024 + 4 t + j)
+
+template <bool kSigned>
+__global__ void __launch_bounds__(kDeqThreads)
 dequantize_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ absmax, int64_t n,
                   float* __restrict__ y, int vec_ok) {
   __shared__ __align__(16) float s_map[kCodes];
@@ -189,23 +242,20 @@ dequantize_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ a
     const int rem = static_cast<int>(rem_in_block(n, base));
     const float am = absmax[b];
     if (vec_ok && rem == BWD_BLOCK) {
-      const uint32_t w0 = __ldcs(reinterpret_cast<const unsigned int*>(codes + base) + tid);
-      const uint32_t w1 = __ldcs(reinterpret_cast<const unsigned int*>(codes + base + 1024) + tid);
-      float4 o0, o1;
-      o0.x = __fmul_rn(s_map[w0 & 0xff], am);
-      o0.y = __fmul_rn(s_map[(w0 >> 8) & 0xff], am);
-      o0.z = __fmul_rn(s_map[(w0 >> 16) & 0xff], am);
-      o0.w = __fmul_rn(s_map[w0 >> 24], am);
-      o1.x = __fmul_rn(s_map[w1 & 0xff], am);
-      o1.y = __fmul_rn(s_map[(w1 >> 8) & 0xff], am);
-      o1.z = __fmul_rn(s_map[(w1 >> 16) & 0xff], am);
-      o1.w = __fmul_rn(s_map[w1 >> 24], am);
-      __stcs(reinterpret_cast<float4*>(y + base) + tid, o0);
-      __stcs(reinterpret_cast<float4*>(y + base + 1024) + tid, o1);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(codes + base + 1024 * h) + tid);
+        float4 o;
+        o.x = __fmul_rn(s_map[byte_of(w, 0)], am);
+        o.y = __fmul_rn(s_map[byte_of(w, 1)], am);
+        o.z = __fmul_rn(s_map[byte_of(w, 2)], am);
+        o.w = __fmul_rn(s_map[byte_of(w, 3)], am);
+        __stcs(reinterpret_cast<float4*>(y + base + 1024 * h) + tid, o);
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int e = slot_index(tid, j);
+        const int e = (j < 4) ? 4 * tid + j : 1024 + 4 * tid + (j - 4);
         if (e < rem) y[base + e] = __fmul_rn(s_map[codes[base + e]], am);
       }
     }
@@ -239,73 +289,83 @@ struct TensorArgs {
   uint8_t* vc;
   float* va;
   int64_t n;
-  int64_t vec;  // all six pointers 16-byte aligned
+  int64_t vec;  // all four element pointers 16-byte aligned
 };
 
 struct AdamArgs {
   int64_t block_start[kMaxTensors + 1];  // prefix sums of per-tensor block counts
   TensorArgs t[kMaxTensors];
   int32_t num_tensors;
-  float b1, omb1, b2, omb2, eps, step_size, bc2s;
+  float b1, omb1, b2, omb2, eps, step_size, inv_bc2s;
 };
 
 static_assert(sizeof(AdamArgs) <= 32764, "kernel parameter space");
 
 template <bool kBf16>
-__device__ __forceinline__ void load_grad_vec(const void* g, int64_t base, int tid, float* out) {
+__device__ __forceinline__ void load_grad4(const void* g, int64_t e, float* out) {
   if (kBf16) {
-    const uint2 a0 = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(g) + base) + tid);
-    const uint2 a1 =
-        __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(g) + base + 1024) + tid);
-    out[0] = __uint_as_float(a0.x << 16);
-    out[1] = __uint_as_float(a0.x & 0xffff0000u);
-    out[2] = __uint_as_float(a0.y << 16);
-    out[3] = __uint_as_float(a0.y & 0xffff0000u);
-    out[4] = __uint_as_float(a1.x << 16);
-    out[5] = __uint_as_float(a1.x & 0xffff0000u);
-    out[6] = __uint_as_float(a1.y << 16);
-    out[7] = __uint_as_float(a1.y & 0xffff0000u);
+    const uint2 a = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(g) + e));
+    out[0] = __uint_as_float(a.x << 16);
+    out[1] = __uint_as_float(a.x & 0xffff0000u);
+    out[2] = __uint_as_float(a.y << 16);
+    out[3] = __uint_as_float(a.y & 0xffff0000u);
   } else {
-    const float4 a0 = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(g) + base) + tid);
-    const float4 a1 =
-        __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(g) + base + 1024) + tid);
-    out[0] = a0.x; out[1] = a0.y; out[2] = a0.z; out[3] = a0.w;
-    out[4] = a1.x; out[5] = a1.y; out[6] = a1.z; out[7] = a1.w;
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(g) + e));
+    out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
   }
 }
 
+// sqrt with at most ~1 ulp error, no branch (PTX sqrt.approx.f32).
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float r;
+  asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Full-range division with at most 2 ulp error, no branch (PTX div.full.f32).
+__device__ __forceinline__ float div_full(float a, float b) {
+  float r;
+  asm("div.full.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
 template <bool kBf16>
-__device__ __forceinline__ float load_grad_one(const void* g, int64_t i) {
+__device__ __forceinline__ float load_grad1(const void* g, int64_t i) {
   if (kBf16) return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(g)[i]) << 16);
   return static_cast<const float*>(g)[i];
 }
 
 template <bool kBf16>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kCta, 3)
 adam8bit_kernel(const __grid_constant__ AdamArgs args) {
-  __shared__ __align__(16) bwd::Tables s_tab;
-  __shared__ float s_red[2][2][kWarps];
-  copy_to_smem(&s_tab, &g_tables, sizeof(bwd::Tables));
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  bwd::Tables& tab = *reinterpret_cast<bwd::Tables*>(smem_raw);
+  __shared__ __align__(16) float s_red[kGroups][2 * 2 * kGroupWarps];
+  copy_to_smem(&tab, &g_tables, kTablesBytes);
   __syncthreads();
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int group = threadIdx.x / kGroup, t = threadIdx.x % kGroup;
   const int nt = args.num_tensors;
   const int64_t total = args.block_start[nt];
-  const int64_t first = blockIdx.x;
-  if (first >= total) return;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kGroups;
+  int64_t gb = static_cast<int64_t>(blockIdx.x) * kGroups + group;
+  if (gb >= total) return;
 
-  // tensor holding global block `first`: the last ti with block_start[ti] <= first
+  // tensor holding global block gb: the last ti with block_start[ti] <= gb
   int lo = 0, hi = nt - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (args.block_start[mid] <= first) lo = mid; else hi = mid - 1;
+    if (args.block_start[mid] <= gb) lo = mid; else hi = mid - 1;
   }
   int ti = lo;
 
   const float b1 = args.b1, omb1 = args.omb1, b2 = args.b2, omb2 = args.omb2;
-  const float eps = args.eps, step_size = args.step_size, bc2s = args.bc2s;
+  const float eps = args.eps, step_size = args.step_size, inv_bc2s = args.inv_bc2s;
+  const float* map_s = tab.map[0];
+  const float* map_u = tab.map[1];
+
   int it = 0;
-  for (int64_t gb = first; gb < total; gb += gridDim.x, ++it) {
+  for (; gb < total; gb += stride, ++it) {
     while (args.block_start[ti + 1] <= gb) ++ti;
     const TensorArgs& T = args.t[ti];
     const int64_t lb = gb - args.block_start[ti];
@@ -315,98 +375,92 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
     const float ma_old = T.ma[lb];
     const float va_old = T.va[lb];
 
-    float p[8], g[8];
-    uint32_t mcode[8], vcode[8];
+    float p[kPer], g[kPer];
+    uint32_t mw[4], vw[4];
     if (vec) {
-      const float4 p0 = __ldcs(reinterpret_cast<const float4*>(T.p + base) + tid);
-      const float4 p1 = __ldcs(reinterpret_cast<const float4*>(T.p + base + 1024) + tid);
-      p[0] = p0.x; p[1] = p0.y; p[2] = p0.z; p[3] = p0.w;
-      p[4] = p1.x; p[5] = p1.y; p[6] = p1.z; p[7] = p1.w;
-      load_grad_vec<kBf16>(T.g, base, tid, g);
-      const uint32_t m0 = __ldcs(reinterpret_cast<const unsigned int*>(T.mc + base) + tid);
-      const uint32_t m1 = __ldcs(reinterpret_cast<const unsigned int*>(T.mc + base + 1024) + tid);
-      const uint32_t v0 = __ldcs(reinterpret_cast<const unsigned int*>(T.vc + base) + tid);
-      const uint32_t v1 = __ldcs(reinterpret_cast<const unsigned int*>(T.vc + base + 1024) + tid);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        mcode[j] = (m0 >> (8 * j)) & 0xffu;
-        mcode[4 + j] = (m1 >> (8 * j)) & 0xffu;
-        vcode[j] = (v0 >> (8 * j)) & 0xffu;
-        vcode[4 + j] = (v1 >> (8 * j)) & 0xffu;
+      for (int k = 0; k < 4; ++k) {
+        const int64_t e = base + 512 * k + 4 * t;
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(T.p + e));
+        p[4 * k] = a.x; p[4 * k + 1] = a.y; p[4 * k + 2] = a.z; p[4 * k + 3] = a.w;
+        load_grad4<kBf16>(T.g, e, &g[4 * k]);
+        mw[k] = __ldcs(reinterpret_cast<const unsigned int*>(T.mc + e));
+        vw[k] = __ldcs(reinterpret_cast<const unsigned int*>(T.vc + e));
       }
     } else {
+      // padding slots: p = g = 0 and the codes of zero, so m = v = 0 there
+      // and the block absmax is unchanged
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int e = slot_index(tid, j);
-        const bool in = e < rem;
-        p[j] = in ? T.p[base + e] : 0.0f;
-        g[j] = in ? load_grad_one<kBf16>(T.g, base + e) : 0.0f;
-        mcode[j] = in ? T.mc[base + e] : 128u;  // padding: code of +0.0
-        vcode[j] = in ? T.vc[base + e] : 0u;
+      for (int k = 0; k < 4; ++k) {
+        uint32_t cm[4], cv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int e = slot(t, 4 * k + j);
+          const bool in = e < rem;
+          p[4 * k + j] = in ? T.p[base + e] : 0.0f;
+          g[4 * k + j] = in ? load_grad1<kBf16>(T.g, base + e) : 0.0f;
+          cm[j] = in ? T.mc[base + e] : 128u;
+          cv[j] = in ? T.vc[base + e] : 0u;
+        }
+        mw[k] = pack4(cm[0], cm[1], cm[2], cm[3]);
+        vw[k] = pack4(cv[0], cv[1], cv[2], cv[3]);
       }
     }
 
-    // dequantize -> Adam in fp32 (operation order fixed, one rounding each)
-    float m[8], v[8];
-    float mmax = 0.0f, vmax = 0.0f;
+    // dequantize -> Adam in fp32.  The moments take one rounding per
+    // operation in the oracle's order, so they (and the codes and absmax
+    // derived from them) are bit-identical; the parameter update uses
+    // branch-free approximate sqrt and division (a few ulps of the update)
+    float m[kPer], v[kPer];
+    float mx[2] = {0.0f, 0.0f};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float m_old = __fmul_rn(s_tab.map[0][mcode[j]], ma_old);
-      const float v_old = __fmul_rn(s_tab.map[1][vcode[j]], va_old);
+    for (int j = 0; j < kPer; ++j) {
+      const float m_old = __fmul_rn(map_s[byte_of(mw[j >> 2], j & 3)], ma_old);
+      const float v_old = __fmul_rn(map_u[byte_of(vw[j >> 2], j & 3)], va_old);
       const float gj = g[j];
       m[j] = __fadd_rn(__fmul_rn(b1, m_old), __fmul_rn(omb1, gj));
       v[j] = __fadd_rn(__fmul_rn(b2, v_old), __fmul_rn(__fmul_rn(omb2, gj), gj));
-      const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v[j]), bc2s), eps);
-      p[j] = __fsub_rn(p[j], __fdiv_rn(__fmul_rn(step_size, m[j]), denom));
-      mmax = fmaxf(mmax, fabsf(m[j]));
-      vmax = fmaxf(vmax, fabsf(v[j]));
+      const float denom = __fadd_rn(__fmul_rn(sqrt_approx(v[j]), inv_bc2s), eps);
+      p[j] = __fsub_rn(p[j], div_full(__fmul_rn(step_size, m[j]), denom));
+      mx[0] = fmaxf(mx[0], fabsf(m[j]));
+      mx[1] = fmaxf(mx[1], v[j]);
     }
-    // padding slots of a partial block (g = 0, codes of zero) give m = v = 0,
-    // so they leave the block absmax unchanged
-
-    // block absmax of the new moments
-    mmax = warp_max(mmax);
-    vmax = warp_max(vmax);
-    if (lane == 0) { s_red[it & 1][0][warp] = mmax; s_red[it & 1][1][warp] = vmax; }
-    __syncthreads();
-    float am = s_red[it & 1][0][0], av = s_red[it & 1][1][0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) {
-      am = fmaxf(am, s_red[it & 1][0][w]);
-      av = fmaxf(av, s_red[it & 1][1][w]);
-    }
-
-    // requantize
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      mcode[j] = (am == 0.0f) ? 128u : quantize_one<true>(m[j], am, s_tab.bkt[0], s_tab.thr[0]);
-      vcode[j] = (av == 0.0f) ? 0u : quantize_one<false>(v[j], av, s_tab.bkt[1], s_tab.thr[1]);
-    }
-
     if (vec) {
-      __stcs(reinterpret_cast<float4*>(T.p + base) + tid, make_float4(p[0], p[1], p[2], p[3]));
-      __stcs(reinterpret_cast<float4*>(T.p + base + 1024) + tid, make_float4(p[4], p[5], p[6], p[7]));
-      __stcs(reinterpret_cast<unsigned int*>(T.mc + base) + tid,
-             mcode[0] | (mcode[1] << 8) | (mcode[2] << 16) | (mcode[3] << 24));
-      __stcs(reinterpret_cast<unsigned int*>(T.mc + base + 1024) + tid,
-             mcode[4] | (mcode[5] << 8) | (mcode[6] << 16) | (mcode[7] << 24));
-      __stcs(reinterpret_cast<unsigned int*>(T.vc + base) + tid,
-             vcode[0] | (vcode[1] << 8) | (vcode[2] << 16) | (vcode[3] << 24));
-      __stcs(reinterpret_cast<unsigned int*>(T.vc + base + 1024) + tid,
-             vcode[4] | (vcode[5] << 8) | (vcode[6] << 16) | (vcode[7] << 24));
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        __stcs(reinterpret_cast<float4*>(T.p + base + 512 * k + 4 * t),
+               make_float4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]));
     } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int e = slot_index(tid, j);
+      for (int j = 0; j < kPer; ++j) {
+        const int e = slot(t, j);
+        if (e < rem) T.p[base + e] = p[j];
+      }
+    }
+
+    // block absmax of the new moments, then requantize
+    group_max<2>(mx, s_red[group], it & 1, group, t);
+    const float am = mx[0], av = mx[1];
+    quantize16<true, false>(m, am, tab, mw);
+    quantize16<false, false>(v, av, tab, vw);
+    if (vec) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        __stcs(reinterpret_cast<unsigned int*>(T.mc + base + 512 * k) + t, mw[k]);
+        __stcs(reinterpret_cast<unsigned int*>(T.vc + base + 512 * k) + t, vw[k]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int e = slot(t, j);
         if (e < rem) {
-          T.p[base + e] = p[j];
-          T.mc[base + e] = static_cast<uint8_t>(mcode[j]);
-          T.vc[base + e] = static_cast<uint8_t>(vcode[j]);
+          T.mc[base + e] = static_cast<uint8_t>(byte_of(mw[j >> 2], j & 3));
+          T.vc[base + e] = static_cast<uint8_t>(byte_of(vw[j >> 2], j & 3));
         }
       }
     }
-    // every thread read the old absmax before the barrier above
-    if (tid == 0) { T.ma[lb] = am; T.va[lb] = av; }
+    // every thread of the group read the old absmax before the barrier above
+    if (t == 0) { T.ma[lb] = am; T.va[lb] = av; }
   }
 }
 
@@ -442,9 +496,16 @@ DeviceState g_dev[kMaxDevices];
 bwd::Tables g_host_tables;
 bool g_host_built = false;
 
-bwd_status occupancy(const void* fn, int* out) {
+// Opts a kernel into `smem` bytes of dynamic shared memory and returns how
+// many of its CTAs fit on one SM.
+bwd_status occupancy(const void* fn, int threads, int smem, int* out) {
   int v = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fn, kThreads, 0);
+  cudaError_t e;
+  if (smem > 0) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
+  }
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fn, threads, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
   *out = v > 0 ? v : 1;
   return BWD_OK;
@@ -470,12 +531,17 @@ bwd_status ensure_device(DeviceState** out) {
   e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
   bwd_status s;
-  if ((s = occupancy(reinterpret_cast<const void*>(quantize_kernel<true>), &d.occ_quant[0])) != BWD_OK) return s;
-  if ((s = occupancy(reinterpret_cast<const void*>(quantize_kernel<false>), &d.occ_quant[1])) != BWD_OK) return s;
-  if ((s = occupancy(reinterpret_cast<const void*>(dequantize_kernel<true>), &d.occ_dequant[0])) != BWD_OK) return s;
-  if ((s = occupancy(reinterpret_cast<const void*>(dequantize_kernel<false>), &d.occ_dequant[1])) != BWD_OK) return s;
-  if ((s = occupancy(reinterpret_cast<const void*>(adam8bit_kernel<false>), &d.occ_adam[0])) != BWD_OK) return s;
-  if ((s = occupancy(reinterpret_cast<const void*>(adam8bit_kernel<true>), &d.occ_adam[1])) != BWD_OK) return s;
+  const void* kq[2] = {reinterpret_cast<const void*>(quantize_kernel<true>),
+                       reinterpret_cast<const void*>(quantize_kernel<false>)};
+  const void* kd[2] = {reinterpret_cast<const void*>(dequantize_kernel<true>),
+                       reinterpret_cast<const void*>(dequantize_kernel<false>)};
+  const void* ka[2] = {reinterpret_cast<const void*>(adam8bit_kernel<false>),
+                       reinterpret_cast<const void*>(adam8bit_kernel<true>)};
+  for (int k = 0; k < 2; ++k) {
+    if ((s = occupancy(kq[k], kCta, kTablesBytes, &d.occ_quant[k])) != BWD_OK) return s;
+    if ((s = occupancy(kd[k], kDeqThreads, 0, &d.occ_dequant[k])) != BWD_OK) return s;
+    if ((s = occupancy(ka[k], kCta, kTablesBytes, &d.occ_adam[k])) != BWD_OK) return s;
+  }
   d.ready = true;
   *out = &d;
   return BWD_OK;
@@ -483,9 +549,12 @@ bwd_status ensure_device(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int grid_for(int64_t blocks, const DeviceState& d, int occ) {
+// CTAs for `blocks` quantization blocks when each CTA works on `per_cta` at a
+// time: enough to cover them, at most one full wave of resident CTAs.
+int grid_for(int64_t blocks, int per_cta, const DeviceState& d, int occ) {
+  const int64_t need = (blocks + per_cta - 1) / per_cta;
   const int64_t cap = static_cast<int64_t>(d.num_sms) * occ;
-  return static_cast<int>(blocks < cap ? blocks : cap);
+  return static_cast<int>(need < cap ? need : cap);
 }
 
 bwd_status check_launch(const char* what) {
@@ -518,15 +587,15 @@ void fill_scalars(const bwd_adam_hparams* hp, AdamArgs* a) {
   a->omb2 = static_cast<float>(1.0 - b2);
   a->eps = hp->eps;
   a->step_size = static_cast<float>(static_cast<double>(hp->lr) / bc1);
-  a->bc2s = static_cast<float>(std::sqrt(bc2));
+  a->inv_bc2s = static_cast<float>(1.0 / std::sqrt(bc2));
 }
 
 bwd_status launch_adam_chunk(const AdamArgs& a, bool bf16, const DeviceState& d, cudaStream_t st) {
   const int64_t total = a.block_start[a.num_tensors];
   if (total == 0) return BWD_OK;
-  const int grid = grid_for(total, d, d.occ_adam[bf16 ? 1 : 0]);
-  if (bf16) adam8bit_kernel<true><<<grid, kThreads, 0, st>>>(a);
-  else adam8bit_kernel<false><<<grid, kThreads, 0, st>>>(a);
+  const int grid = grid_for(total, kGroups, d, d.occ_adam[bf16 ? 1 : 0]);
+  if (bf16) adam8bit_kernel<true><<<grid, kCta, kTablesBytes, st>>>(a);
+  else adam8bit_kernel<false><<<grid, kCta, kTablesBytes, st>>>(a);
   return check_launch("adam8bit_kernel launch");
 }
 
@@ -567,9 +636,11 @@ bwd_status bwd_quantize_blockwise(const float* x, int64_t n, bwd_map_kind kind, 
   const int vec = aligned16(x) && aligned16(codes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (kind == BWD_MAP_SIGNED)
-    quantize_kernel<true><<<grid_for(nb, *d, d->occ_quant[0]), kThreads, 0, st>>>(x, n, codes, absmax, vec);
+    quantize_kernel<true><<<grid_for(nb, kGroups, *d, d->occ_quant[0]), kCta, kTablesBytes, st>>>(
+        x, n, codes, absmax, vec);
   else
-    quantize_kernel<false><<<grid_for(nb, *d, d->occ_quant[1]), kThreads, 0, st>>>(x, n, codes, absmax, vec);
+    quantize_kernel<false><<<grid_for(nb, kGroups, *d, d->occ_quant[1]), kCta, kTablesBytes, st>>>(
+        x, n, codes, absmax, vec);
   return check_launch("quantize_kernel launch");
 }
 
@@ -586,9 +657,11 @@ bwd_status bwd_dequantize_blockwise(const uint8_t* codes, const float* absmax, i
   const int vec = aligned16(codes) && aligned16(y);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (kind == BWD_MAP_SIGNED)
-    dequantize_kernel<true><<<grid_for(nb, *d, d->occ_dequant[0]), kThreads, 0, st>>>(codes, absmax, n, y, vec);
+    dequantize_kernel<true><<<grid_for(nb, 1, *d, d->occ_dequant[0]), kDeqThreads, 0, st>>>(
+        codes, absmax, n, y, vec);
   else
-    dequantize_kernel<false><<<grid_for(nb, *d, d->occ_dequant[1]), kThreads, 0, st>>>(codes, absmax, n, y, vec);
+    dequantize_kernel<false><<<grid_for(nb, 1, *d, d->occ_dequant[1]), kDeqThreads, 0, st>>>(
+        codes, absmax, n, y, vec);
   return check_launch("dequantize_kernel launch");
 }
 
@@ -600,9 +673,9 @@ bwd_status bwd_state_init(uint8_t* m_codes, float* m_absmax, uint8_t* v_codes, f
   DeviceState* d = nullptr;
   bwd_status s = ensure_device(&d);
   if (s != BWD_OK) return s;
-  const int64_t work = (n + kThreads - 1) / kThreads;
+  const int64_t work = (n + kDeqThreads - 1) / kDeqThreads;
   const int grid = static_cast<int>(work < d->num_sms * 8 ? work : d->num_sms * 8);
-  fill_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+  fill_kernel<<<grid, kDeqThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       m_codes, 128, v_codes, 0, n, m_absmax, v_absmax, bwd_num_blocks(n));
   return check_launch("fill_kernel launch");
 }

@@ -4,9 +4,11 @@ QUANTIZATION").
 
 Tolerance of a step taken from identical input state: parameters rtol 1e-5,
 atol 1e-7; at most 1e-4 of the codes may differ, each by at most one index;
-absmax rtol 1e-6.  The kernel performs the same binary32 operations in the
-same order as the oracle, so in practice every output is bit-identical; the
-tests also record that exactness."""
+absmax rtol 1e-6.  The kernel computes the moments with the same binary32
+operations in the same order as the oracle, so the codes and absmax of the
+new state are bit-identical, and the tests assert that as well; the
+parameter update uses approximate sqrt and division and stays within a few
+ulps of the update term, far inside the parameter tolerance."""
 
 import numpy as np
 import pytest
@@ -51,8 +53,9 @@ def compare_step(gpu, ref, exact=True):
         assert np.count_nonzero(d) <= max(1e-4 * c.size, 0)
     np.testing.assert_allclose(ma, rma, rtol=1e-6, atol=0)
     np.testing.assert_allclose(va, rva, rtol=1e-6, atol=0)
+    # the update term is at most ~lr; its few-ulp error bounds |p - rp|
+    assert np.all(np.abs(p.astype(np.float64) - rp) <= 3e-8 + 4e-7 * np.abs(rp))
     if exact:
-        assert np.array_equal(p.view(U32), rp.view(U32))
         assert np.array_equal(mc, rmc) and np.array_equal(vc, rvc)
         assert np.array_equal(ma.view(U32), rma.view(U32)) and np.array_equal(va.view(U32), rva.view(U32))
 
