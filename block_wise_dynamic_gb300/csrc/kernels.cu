@@ -9,11 +9,13 @@
 // stores them quantized again.
 //
 // Work decomposition.  A group of 128 threads owns one 2048-element block at a
-// time; a CTA holds two groups and the groups walk the blocks with a grid
-// stride (grid = SMs x resident CTAs).  Thread t of a group owns the 16
-// elements 4 t + 512 k + j (k, j < 4) of its block, so every warp-wide load or
-// store touches one contiguous span (512 B of fp32, 256 B of bf16, 128 B of
-// codes) and is fully coalesced.  The block absmax is a warp shuffle
+// time; a CTA holds two groups (four in the standalone quantizer, which
+// needs fewer registers) and the groups walk the blocks with a grid stride
+// (grid = SMs x resident CTAs).  Thread t of a group owns the 16
+// elements 4 t + 512 k + j (k, j < 4) of its block ("quads" of 4 elements,
+// 4 x 128 = 512 elements apart), so every warp-wide load or store touches one
+// contiguous span (512 B of fp32, 256 B of bf16, 128 B of codes) and is fully
+// coalesced.  The block absmax is a warp shuffle
 // reduction and a pass over the group's four warps through shared memory,
 // synchronised by a named barrier per group.  The maps, thresholds and the
 // count table (tables.h) are copied once per CTA into dynamic shared memory.
@@ -44,15 +46,19 @@ using bwd::kCodes;
 
 constexpr int kGroup = 128;                   // threads per 2048-element block
 constexpr int kPer = BWD_BLOCK / kGroup;      // 16 elements per thread
+constexpr int kQuads = kPer / 4;              // 4-element quads per thread
+constexpr int kSpan = 4 * kGroup;             // elements between a thread's quads
 constexpr int kGroupWarps = kGroup / 32;      // 4
-constexpr int kGroups = 2;                    // blocks in flight per CTA
+constexpr int kGroups = 2;                    // blocks in flight per CTA (Adam)
 constexpr int kCta = kGroup * kGroups;        // 256 threads
+constexpr int kQGroups = 4;                   // blocks in flight per CTA (quantize)
+constexpr int kQCta = kGroup * kQGroups;      // 512 threads
 constexpr int kDeqThreads = 256;              // dequantize: 8 elements per thread
 constexpr int kMaxTensors = 448;              // per launch, bounded by kernel parameter space
 constexpr int kMaxDevices = 64;
 constexpr int kTablesBytes = static_cast<int>(sizeof(bwd::Tables));
 
-static_assert(kPer == 16, "the element layout below assumes 16 elements per thread");
+static_assert(kPer % 4 == 0 && kGroupWarps % 4 == 0, "quads of 4 elements, partials read as float4");
 
 __device__ bwd::Tables g_tables;  // immutable after the first upload per device
 
@@ -71,7 +77,7 @@ __device__ __forceinline__ void group_sync(int group) {
 }
 
 // Element of the block owned by slot j (0..15) of thread t.
-__device__ __forceinline__ int slot(int t, int j) { return 4 * t + 512 * (j >> 2) + (j & 3); }
+__device__ __forceinline__ int slot(int t, int j) { return 4 * t + kSpan * (j >> 2) + (j & 3); }
 
 __device__ __forceinline__ int64_t rem_in_block(int64_t n, int64_t base) {
   const int64_t r = n - base;
@@ -114,10 +120,13 @@ __device__ __forceinline__ uint32_t code_unsigned(float q, const bwd::Tables& ta
 // line (one exact quotient per value from the block's reciprocal, see
 // exact_div.cuh).  Quotients of magnitude below 2^-99 may be off there; only a
 // negative one can change a code (-0.0 -> code 128, a negative subnormal ->
-// code 127), so those are flagged and redone with IEEE division afterwards.
+// code 127).  Read as signed integers, the bit patterns of -0.0 and of the
+// negative values closest to zero are the smallest of all, so one integer
+// min over the quotients flags a block that has one; its values are then
+// redone with IEEE division.
 template <bool kSigned, bool kAnySign>
-__device__ __forceinline__ void quantize16(const float (&x)[kPer], float a, const bwd::Tables& tab,
-                                           uint32_t (&w)[4]) {
+__device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, const bwd::Tables& tab,
+                                           uint32_t (&w)[kQuads]) {
   uint32_t c[kPer];
   if (a == 0.0f) {
 #pragma unroll
@@ -125,14 +134,14 @@ __device__ __forceinline__ void quantize16(const float (&x)[kPer], float a, cons
   } else {
     const bwd::Divisor d = bwd::make_divisor(a, 1u);
     if (d.fast) {
-      bool fix = false;
+      int minb = 0x7fffffff;
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
         const float q = bwd::div_fast(d, x[j]);
-        if (kSigned) fix |= (x[j] < 0.0f) & (q > -0x1p-99f);
+        if (kSigned) minb = min(minb, __float_as_int(q));
         c[j] = kSigned ? code_signed(q, tab) : (kAnySign ? code_unsigned(q, tab) : code_unsigned_nonneg(q, tab));
       }
-      if (kSigned && fix) {
+      if (kSigned && minb <= static_cast<int>(0x8E000000u)) {
 #pragma unroll
         for (int j = 0; j < kPer; ++j)
           if (x[j] < 0.0f && bwd::div_fast(d, x[j]) > -0x1p-99f) c[j] = code_signed(__fdiv_rn(x[j], a), tab);
@@ -146,7 +155,7 @@ __device__ __forceinline__ void quantize16(const float (&x)[kPer], float a, cons
     }
   }
 #pragma unroll
-  for (int k = 0; k < 4; ++k) w[k] = pack4(c[4 * k], c[4 * k + 1], c[4 * k + 2], c[4 * k + 3]);
+  for (int k = 0; k < kQuads; ++k) w[k] = pack4(c[4 * k], c[4 * k + 1], c[4 * k + 2], c[4 * k + 3]);
 }
 
 // Max over the 128 threads of a group; every thread gets the result.
@@ -163,8 +172,13 @@ __device__ __forceinline__ void group_max(float (&v)[kVals], float* red, int par
   group_sync(group);
 #pragma unroll
   for (int i = 0; i < kVals; ++i) {
-    const float4 r = *reinterpret_cast<const float4*>(&red[(parity * kVals + i) * kGroupWarps]);
-    v[i] = fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w));
+    float mx = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kGroupWarps; q += 4) {
+      const float4 r = *reinterpret_cast<const float4*>(&red[(parity * kVals + i) * kGroupWarps + q]);
+      mx = fmaxf(mx, fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w)));
+    }
+    v[i] = mx;
   }
 }
 
@@ -172,28 +186,28 @@ __device__ __forceinline__ void group_max(float (&v)[kVals], float* red, int par
 // quantize
 
 template <bool kSigned>
-__global__ void __launch_bounds__(kCta, 4)
+__global__ void __launch_bounds__(kQCta, 2)
 quantize_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ codes,
                 float* __restrict__ absmax, int vec_ok) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   bwd::Tables& tab = *reinterpret_cast<bwd::Tables*>(smem_raw);
-  __shared__ __align__(16) float s_red[kGroups][2 * kGroupWarps];
+  __shared__ __align__(16) float s_red[kQGroups][2 * kGroupWarps];
   copy_to_smem(&tab, &g_tables, kTablesBytes);
   __syncthreads();
 
   const int group = threadIdx.x / kGroup, t = threadIdx.x % kGroup;
   const int64_t nb = (n + BWD_BLOCK - 1) / BWD_BLOCK;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kGroups;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kQGroups;
   int it = 0;
-  for (int64_t b = static_cast<int64_t>(blockIdx.x) * kGroups + group; b < nb; b += stride, ++it) {
+  for (int64_t b = static_cast<int64_t>(blockIdx.x) * kQGroups + group; b < nb; b += stride, ++it) {
     const int64_t base = b * BWD_BLOCK;
     const int rem = static_cast<int>(rem_in_block(n, base));
     const bool vec = vec_ok && rem == BWD_BLOCK;
     float v[kPer];
     if (vec) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(x + base + 512 * k) + t);
+      for (int k = 0; k < kQuads; ++k) {
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(x + base + kSpan * k) + t);
         v[4 * k] = a.x; v[4 * k + 1] = a.y; v[4 * k + 2] = a.z; v[4 * k + 3] = a.w;
       }
     } else {
@@ -209,11 +223,11 @@ quantize_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ co
     group_max<1>(mx, s_red[group], it & 1, group, t);
     const float am = mx[0];
 
-    uint32_t w[4];
-    quantize16<kSigned, true>(v, am, tab, w);
+    uint32_t w[kQuads];
+    quantize_quads<kSigned, true>(v, am, tab, w);
     if (vec) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) __stcs(reinterpret_cast<unsigned int*>(codes + base + 512 * k) + t, w[k]);
+      for (int k = 0; k < kQuads; ++k) __stcs(reinterpret_cast<unsigned int*>(codes + base + kSpan * k) + t, w[k]);
     } else {
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
@@ -315,17 +329,17 @@ __device__ __forceinline__ void load_grad4(const void* g, int64_t e, float* out)
   }
 }
 
-// sqrt with at most ~1 ulp error, no branch (PTX sqrt.approx.f32).
-__device__ __forceinline__ float sqrt_approx(float x) {
+// Branch-free approximate reciprocal square root and reciprocal (PTX
+// rsqrt.approx / rcp.approx, a few ulps; inputs here are normal numbers).
+__device__ __forceinline__ float rsqrt_approx(float x) {
   float r;
-  asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
-// Full-range division with at most 2 ulp error, no branch (PTX div.full.f32).
-__device__ __forceinline__ float div_full(float a, float b) {
+__device__ __forceinline__ float rcp_approx(float x) {
   float r;
-  asm("div.full.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
@@ -376,11 +390,11 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
     const float va_old = T.va[lb];
 
     float p[kPer], g[kPer];
-    uint32_t mw[4], vw[4];
+    uint32_t mw[kQuads], vw[kQuads];
     if (vec) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int64_t e = base + 512 * k + 4 * t;
+      for (int k = 0; k < kQuads; ++k) {
+        const int64_t e = base + kSpan * k + 4 * t;
         const float4 a = __ldcs(reinterpret_cast<const float4*>(T.p + e));
         p[4 * k] = a.x; p[4 * k + 1] = a.y; p[4 * k + 2] = a.z; p[4 * k + 3] = a.w;
         load_grad4<kBf16>(T.g, e, &g[4 * k]);
@@ -391,7 +405,7 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
       // padding slots: p = g = 0 and the codes of zero, so m = v = 0 there
       // and the block absmax is unchanged
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kQuads; ++k) {
         uint32_t cm[4], cv[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -420,15 +434,18 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
       const float gj = g[j];
       m[j] = __fadd_rn(__fmul_rn(b1, m_old), __fmul_rn(omb1, gj));
       v[j] = __fadd_rn(__fmul_rn(b2, v_old), __fmul_rn(__fmul_rn(omb2, gj), gj));
-      const float denom = __fadd_rn(__fmul_rn(sqrt_approx(v[j]), inv_bc2s), eps);
-      p[j] = __fsub_rn(p[j], div_full(__fmul_rn(step_size, m[j]), denom));
+      // sqrt(v) = v * rsqrt(v); the 1e-37 keeps rsqrt finite at v = 0 and
+      // does not change sqrt(v) / bc2s + eps for any v that matters
+      const float rs = rsqrt_approx(__fadd_rn(v[j], 1e-37f));
+      const float denom = __fadd_rn(__fmul_rn(__fmul_rn(v[j], rs), inv_bc2s), eps);
+      p[j] = __fsub_rn(p[j], __fmul_rn(__fmul_rn(step_size, m[j]), rcp_approx(denom)));
       mx[0] = fmaxf(mx[0], fabsf(m[j]));
       mx[1] = fmaxf(mx[1], v[j]);
     }
     if (vec) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        __stcs(reinterpret_cast<float4*>(T.p + base + 512 * k + 4 * t),
+      for (int k = 0; k < kQuads; ++k)
+        __stcs(reinterpret_cast<float4*>(T.p + base + kSpan * k + 4 * t),
                make_float4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]));
     } else {
 #pragma unroll
@@ -441,13 +458,13 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
     // block absmax of the new moments, then requantize
     group_max<2>(mx, s_red[group], it & 1, group, t);
     const float am = mx[0], av = mx[1];
-    quantize16<true, false>(m, am, tab, mw);
-    quantize16<false, false>(v, av, tab, vw);
+    quantize_quads<true, false>(m, am, tab, mw);
+    quantize_quads<false, false>(v, av, tab, vw);
     if (vec) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        __stcs(reinterpret_cast<unsigned int*>(T.mc + base + 512 * k) + t, mw[k]);
-        __stcs(reinterpret_cast<unsigned int*>(T.vc + base + 512 * k) + t, vw[k]);
+      for (int k = 0; k < kQuads; ++k) {
+        __stcs(reinterpret_cast<unsigned int*>(T.mc + base + kSpan * k) + t, mw[k]);
+        __stcs(reinterpret_cast<unsigned int*>(T.vc + base + kSpan * k) + t, vw[k]);
       }
     } else {
 #pragma unroll
@@ -538,7 +555,7 @@ bwd_status ensure_device(DeviceState** out) {
   const void* ka[2] = {reinterpret_cast<const void*>(adam8bit_kernel<false>),
                        reinterpret_cast<const void*>(adam8bit_kernel<true>)};
   for (int k = 0; k < 2; ++k) {
-    if ((s = occupancy(kq[k], kCta, kTablesBytes, &d.occ_quant[k])) != BWD_OK) return s;
+    if ((s = occupancy(kq[k], kQCta, kTablesBytes, &d.occ_quant[k])) != BWD_OK) return s;
     if ((s = occupancy(kd[k], kDeqThreads, 0, &d.occ_dequant[k])) != BWD_OK) return s;
     if ((s = occupancy(ka[k], kCta, kTablesBytes, &d.occ_adam[k])) != BWD_OK) return s;
   }
@@ -636,10 +653,10 @@ bwd_status bwd_quantize_blockwise(const float* x, int64_t n, bwd_map_kind kind, 
   const int vec = aligned16(x) && aligned16(codes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (kind == BWD_MAP_SIGNED)
-    quantize_kernel<true><<<grid_for(nb, kGroups, *d, d->occ_quant[0]), kCta, kTablesBytes, st>>>(
+    quantize_kernel<true><<<grid_for(nb, kQGroups, *d, d->occ_quant[0]), kQCta, kTablesBytes, st>>>(
         x, n, codes, absmax, vec);
   else
-    quantize_kernel<false><<<grid_for(nb, kGroups, *d, d->occ_quant[1]), kCta, kTablesBytes, st>>>(
+    quantize_kernel<false><<<grid_for(nb, kQGroups, *d, d->occ_quant[1]), kQCta, kTablesBytes, st>>>(
         x, n, codes, absmax, vec);
   return check_launch("quantize_kernel launch");
 }
