@@ -1,4 +1,4 @@
-// Host builder of the dynamic-tree maps, thresholds and bucket tables.
+// Host builder of the dynamic-tree maps, thresholds and the count table.
 //
 // "8-BIT OPTIMIZERS VIA BLOCK-WISE QUANTIZATION", section 二 / 动态量化: an
 // 8-bit dynamic tree number is a sign bit, an exponent counted as leading
@@ -91,17 +91,21 @@ int fill_bucket(const float* t, float v_lo, float v_hi, uint8_t* out, char* err,
 }
 
 int build_counts(const float* ts, const float* tu, uint8_t* cnt, char* err, size_t errlen) {
-  std::memset(cnt, 255, kCntPad);
-  for (uint32_t i = 0; i <= kCntUnsignedMax; ++i) {
+  std::memset(cnt, 255, kCntPad);  // buckets no normalised value reaches
+  const uint32_t sh = kCntSignedShift, low = (1u << kCntSignedShift) - 1u;
+  for (uint32_t i = 0; i <= (kCntSignedMax & 0x1fffu); ++i) {
     // non-negative patterns: the lowest value has the smallest pattern
-    const float lo = from_bits(i << 16), hi = from_bits((i << 16) | 0xffffu);
-    if (fill_bucket(ts, lo, hi, &cnt[i], err, errlen) != 0) return -1;
-    if (fill_bucket(tu, lo, hi, &cnt[i + kCntUnsignedOff], err, errlen) != 0) return -1;
-  }
-  for (uint32_t i = 0x8000u; i <= kCntSignedMax; ++i) {
+    if (fill_bucket(ts, from_bits(i << sh), from_bits((i << sh) | low), &cnt[i], err, errlen) != 0) return -1;
     // negative patterns: the lowest value has the largest pattern
-    const float lo = from_bits((i << 16) | 0xffffu), hi = from_bits(i << 16);
-    if (fill_bucket(ts, lo, hi, &cnt[i], err, errlen) != 0) return -1;
+    const uint32_t n = i | 0x4000u;
+    if (fill_bucket(ts, from_bits((n << sh) | low), from_bits(n << sh), &cnt[n], err, errlen) != 0) return -1;
+  }
+  for (uint32_t h = kCntUnsignedLo; h <= kCntUnsignedHi; ++h) {
+    // the first bucket also takes every value below 2^-26
+    const float lo = h == kCntUnsignedLo ? 0.0f : from_bits(h << 16);
+    if (fill_bucket(tu, lo, from_bits((h << 16) | 0xffffu), &cnt[kCntUnsignedOff + h - kCntUnsignedLo], err,
+                    errlen) != 0)
+      return -1;
   }
   return 0;
 }

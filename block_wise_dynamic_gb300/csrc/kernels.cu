@@ -96,16 +96,38 @@ __device__ __forceinline__ void copy_to_smem(void* dst, const void* src, int byt
   for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x) d[i] = s[i];
 }
 
-// Code of a normalised value (see the count table in tables.h).  The clamp
-// keeps any bit pattern, non-finite ones included, inside the table.
+// Streaming global loads that bypass L1 allocation (each byte is read
+// once): L1 capacity stays free for the requests in flight.
+__device__ __forceinline__ float4 ld_stream_f4(const void* p) {
+  float4 r;
+  asm volatile("ld.global.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u1(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+// Code of a normalised value (see the count tables in tables.h).  The clamps
+// keep any bit pattern, non-finite ones included, inside the tables.
 __device__ __forceinline__ uint32_t code_signed(float q, const bwd::Tables& tab) {
-  const uint32_t c = tab.cnt[min(__float_as_uint(q) >> 16, bwd::kCntSignedMax)];
+  const uint32_t c = tab.cnt[min(__float_as_uint(q) >> bwd::kCntSignedShift, bwd::kCntSignedMax)];
   return c + (tab.thr[0][c] <= q ? 1u : 0u);
 }
 
 // Unsigned map, q >= +0 (the second moment is never negative).
 __device__ __forceinline__ uint32_t code_unsigned_nonneg(float q, const bwd::Tables& tab) {
-  const uint32_t c = tab.cnt[min(__float_as_uint(q) >> 16, bwd::kCntUnsignedMax) + bwd::kCntUnsignedOff];
+  const uint32_t h = min(max(__float_as_uint(q) >> 16, bwd::kCntUnsignedLo), bwd::kCntUnsignedHi);
+  const uint32_t c = tab.cnt[h + (bwd::kCntUnsignedOff - bwd::kCntUnsignedLo)];
   return c + (tab.thr[1][c] <= q ? 1u : 0u);
 }
 
@@ -207,7 +229,7 @@ quantize_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ co
     if (vec) {
 #pragma unroll
       for (int k = 0; k < kQuads; ++k) {
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(x + base + kSpan * k) + t);
+        const float4 a = ld_stream_f4(x + base + kSpan * k + 4 * t);
         v[4 * k] = a.x; v[4 * k + 1] = a.y; v[4 * k + 2] = a.z; v[4 * k + 3] = a.w;
       }
     } else {
@@ -318,13 +340,13 @@ static_assert(sizeof(AdamArgs) <= 32764, "kernel parameter space");
 template <bool kBf16>
 __device__ __forceinline__ void load_grad4(const void* g, int64_t e, float* out) {
   if (kBf16) {
-    const uint2 a = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(g) + e));
+    const uint2 a = ld_stream_u2(static_cast<const uint16_t*>(g) + e);
     out[0] = __uint_as_float(a.x << 16);
     out[1] = __uint_as_float(a.x & 0xffff0000u);
     out[2] = __uint_as_float(a.y << 16);
     out[3] = __uint_as_float(a.y & 0xffff0000u);
   } else {
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(g) + e));
+    const float4 a = ld_stream_f4(static_cast<const float*>(g) + e);
     out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
   }
 }
@@ -395,11 +417,11 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
 #pragma unroll
       for (int k = 0; k < kQuads; ++k) {
         const int64_t e = base + kSpan * k + 4 * t;
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(T.p + e));
+        const float4 a = ld_stream_f4(T.p + e);
         p[4 * k] = a.x; p[4 * k + 1] = a.y; p[4 * k + 2] = a.z; p[4 * k + 3] = a.w;
         load_grad4<kBf16>(T.g, e, &g[4 * k]);
-        mw[k] = __ldcs(reinterpret_cast<const unsigned int*>(T.mc + e));
-        vw[k] = __ldcs(reinterpret_cast<const unsigned int*>(T.vc + e));
+        mw[k] = ld_stream_u1(T.mc + e);
+        vw[k] = ld_stream_u1(T.vc + e);
       }
     } else {
       // padding slots: p = g = 0 and the codes of zero, so m = v = 0 there
@@ -437,8 +459,8 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
       // sqrt(v) = v * rsqrt(v); the 1e-37 keeps rsqrt finite at v = 0 and
       // does not change sqrt(v) / bc2s + eps for any v that matters
       const float rs = rsqrt_approx(__fadd_rn(v[j], 1e-37f));
-      const float denom = __fadd_rn(__fmul_rn(__fmul_rn(v[j], rs), inv_bc2s), eps);
-      p[j] = __fsub_rn(p[j], __fmul_rn(__fmul_rn(step_size, m[j]), rcp_approx(denom)));
+      const float denom = __fmaf_rn(__fmul_rn(v[j], rs), inv_bc2s, eps);
+      p[j] = __fmaf_rn(-__fmul_rn(step_size, m[j]), rcp_approx(denom), p[j]);
       mx[0] = fmaxf(mx[0], fabsf(m[j]));
       mx[1] = fmaxf(mx[1], v[j]);
     }
