@@ -63,6 +63,19 @@ def dist_info():
     return world, rank, local
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The slowest rank's value (all ranks get it); x itself without a
+    process group."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # --------------------------------------------------------------------------
 # clocks during the timed region
 
@@ -297,10 +310,7 @@ def run_ours(args):
     clocks.stop()
     elapsed_ms = e0.elapsed_time(e1)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     # end to end through the public API with host buffers: the step's
     # gradients arrive from pinned host memory and the updated parameters go
@@ -311,6 +321,8 @@ def run_ours(args):
         e2e = {"value": None, "unit": "params/s", "h2d_bytes_per_step": N * gbytes, "d2h_bytes_per_step": N * 4,
                "skipped": f"needs {pinned_bytes / 1e9:.0f} GB of pinned host memory per rank"}
     elif args.e2e_steps > 0:
+        from block_wise_dynamic_gb300.offload import PipelinedHostStep
+
         gh = torch.empty(N, dtype=wl.grad_dtype, pin_memory=True)
         ph = torch.empty(N, dtype=torch.float32, pin_memory=True)
         off = 0
@@ -320,6 +332,8 @@ def run_ours(args):
             phv.append(ph[off:off + n])
             ghv[-1].copy_(gs[i])
             off += n
+        pipe = PipelinedHostStep(ps, gs, *[[s[k] for s in sts] for k in range(4)], ghv, phv,
+                                 chunk_bytes=512 << 20)
         torch.cuda.synchronize(dev)
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
@@ -327,25 +341,19 @@ def run_ours(args):
         f0.record(stream)
         for _ in range(args.e2e_steps):
             t += 1
-            for i in range(len(sizes)):
-                gs[i].copy_(ghv[i], non_blocking=True)
-            mt.step(step=t, **hp)
-            for i in range(len(sizes)):
-                phv[i].copy_(ps[i], non_blocking=True)
+            pipe.step(step=t, **hp)
         f1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
         e2e_ms = f0.elapsed_time(f1)
-        if world > 1:
-            tt = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(e2e_ms, dev)
         e2e = {"value": world * N * args.e2e_steps / (e2e_ms / 1e3), "unit": "params/s",
                "h2d_bytes_per_step": N * gbytes, "d2h_bytes_per_step": N * 4,
                "steps": args.e2e_steps,
-               "what": "per step: H2D of all gradients from pinned host memory, the multi-tensor step, "
-                       "D2H of all updated fp32 parameters into pinned host memory, one stream"}
-        del gh, ph, ghv, phv
+               "what": "per step through block_wise_dynamic_gb300.offload.PipelinedHostStep: gradients "
+                       "H2D from pinned host memory, the 8-bit step, updated fp32 parameters D2H into "
+                       "pinned host memory, pipelined over 512 MiB chunks on three streams"}
+        del gh, ph, ghv, phv, pipe
 
     if rank != 0:
         if world > 1:
@@ -479,10 +487,7 @@ def run_quant(args):
     c1 = time.perf_counter()
     clocks.stop()
     elapsed_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
     per_pass = {}
     for j, (name, _) in enumerate(passes):
         ms = statistics.fmean(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(args.steps))

@@ -33,6 +33,7 @@ __all__ = [
     "adam8bit_step_multi",
     "MultiTensorArgs",
     "Adam8bit",
+    "AdamW8bit",
 ]
 
 _KINDS = {"signed": _abi.BWD_MAP_SIGNED, "unsigned": _abi.BWD_MAP_UNSIGNED}
@@ -151,8 +152,9 @@ def _hparams(lr, beta1, beta2, eps, step, weight_decay=0.0) -> _abi.AdamHParams:
 
 
 def adam8bit_step(p, g, m_codes, m_absmax, v_codes, v_absmax, *, lr=1e-3, beta1=0.9, beta2=0.999,
-                  eps=1e-8, step, stream=None) -> None:
-    """One 8-bit Adam step on one flat tensor, in place (``bwd_adam8bit_step``)."""
+                  eps=1e-8, weight_decay=0.0, step, stream=None) -> None:
+    """One 8-bit Adam step on one flat tensor, in place (``bwd_adam8bit_step``);
+    ``weight_decay`` > 0 makes it AdamW (decoupled)."""
     n = p.numel()
     _need(p, "p", torch.float32)
     if g.dtype not in _GDT:
@@ -162,7 +164,7 @@ def adam8bit_step(p, g, m_codes, m_absmax, v_codes, v_absmax, *, lr=1e-3, beta1=
     _need(v_codes, "v_codes", torch.uint8, n)
     _need(m_absmax, "m_absmax", torch.float32, num_blocks(n))
     _need(v_absmax, "v_absmax", torch.float32, num_blocks(n))
-    hp = _hparams(lr, beta1, beta2, eps, step)
+    hp = _hparams(lr, beta1, beta2, eps, step, weight_decay)
     with torch.cuda.device(p.device):
         st = _lib.bwd_adam8bit_step(
             p.data_ptr(), g.data_ptr(), _GDT[g.dtype], m_codes.data_ptr(), m_absmax.data_ptr(),
@@ -206,10 +208,11 @@ class MultiTensorArgs:
         self.n = (ctypes.c_int64 * T)(*[t.numel() for t in params])
         self.numel = int(sum(t.numel() for t in params))
 
-    def step(self, *, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, step, stream=None) -> None:
+    def step(self, *, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step,
+             stream=None) -> None:
         if self.T == 0:
             return
-        hp = _hparams(lr, beta1, beta2, eps, step)
+        hp = _hparams(lr, beta1, beta2, eps, step, weight_decay)
         with torch.cuda.device(self.device):
             st = _lib.bwd_adam8bit_step_multi(
                 self.T, self.p, self.g, self.g_dtype, self.mc, self.ma, self.vc, self.va, self.n,
@@ -219,11 +222,11 @@ class MultiTensorArgs:
 
 
 def adam8bit_step_multi(params, grads, m_codes, m_absmax, v_codes, v_absmax, *, lr=1e-3, beta1=0.9,
-                        beta2=0.999, eps=1e-8, step, stream=None) -> None:
-    """One 8-bit Adam step over a list of tensors (``bwd_adam8bit_step_multi``)."""
+                        beta2=0.999, eps=1e-8, weight_decay=0.0, step, stream=None) -> None:
+    """One 8-bit Adam(W) step over a list of tensors (``bwd_adam8bit_step_multi``)."""
     MultiTensorArgs(params, grads, m_codes, m_absmax, v_codes, v_absmax).step(
-        lr=lr, beta1=beta1, beta2=beta2, eps=eps, step=step, stream=stream
+        lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay, step=step, stream=stream
     )
 
 
-from .optim import Adam8bit  # noqa: E402
+from .optim import Adam8bit, AdamW8bit  # noqa: E402

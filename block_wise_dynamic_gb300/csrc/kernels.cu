@@ -333,6 +333,7 @@ struct AdamArgs {
   TensorArgs t[kMaxTensors];
   int32_t num_tensors;
   float b1, omb1, b2, omb2, eps, step_size, inv_bc2s;
+  float decay;  // 1 - lr * weight_decay (decoupled weight decay), 1 for Adam
 };
 
 static_assert(sizeof(AdamArgs) <= 32764, "kernel parameter space");
@@ -396,7 +397,7 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
   int ti = lo;
 
   const float b1 = args.b1, omb1 = args.omb1, b2 = args.b2, omb2 = args.omb2;
-  const float eps = args.eps, step_size = args.step_size, inv_bc2s = args.inv_bc2s;
+  const float eps = args.eps, step_size = args.step_size, inv_bc2s = args.inv_bc2s, decay = args.decay;
   const float* map_s = tab.map[0];
   const float* map_u = tab.map[1];
 
@@ -460,7 +461,7 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
       // does not change sqrt(v) / bc2s + eps for any v that matters
       const float rs = rsqrt_approx(__fadd_rn(v[j], 1e-37f));
       const float denom = __fmaf_rn(__fmul_rn(v[j], rs), inv_bc2s, eps);
-      p[j] = __fmaf_rn(-__fmul_rn(step_size, m[j]), rcp_approx(denom), p[j]);
+      p[j] = __fmaf_rn(-__fmul_rn(step_size, m[j]), rcp_approx(denom), __fmul_rn(p[j], decay));
       mx[0] = fmaxf(mx[0], fabsf(m[j]));
       mx[1] = fmaxf(mx[1], v[j]);
     }
@@ -611,7 +612,8 @@ bwd_status check_hparams(const bwd_adam_hparams* hp) {
     return fail(BWD_ERR_INVALID_ARG, "lr and eps must be finite, eps >= 0");
   if (!(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
     return fail(BWD_ERR_INVALID_ARG, "betas must lie in [0, 1)");
-  if (hp->weight_decay != 0.0f) return fail(BWD_ERR_INVALID_ARG, "weight_decay must be 0");
+  if (!std::isfinite(hp->weight_decay) || hp->weight_decay < 0.0f)
+    return fail(BWD_ERR_INVALID_ARG, "weight_decay must be finite and >= 0");
   return BWD_OK;
 }
 
@@ -627,6 +629,7 @@ void fill_scalars(const bwd_adam_hparams* hp, AdamArgs* a) {
   a->eps = hp->eps;
   a->step_size = static_cast<float>(static_cast<double>(hp->lr) / bc1);
   a->inv_bc2s = static_cast<float>(1.0 / std::sqrt(bc2));
+  a->decay = static_cast<float>(1.0 - static_cast<double>(hp->lr) * static_cast<double>(hp->weight_decay));
 }
 
 bwd_status launch_adam_chunk(const AdamArgs& a, bool bf16, const DeviceState& d, cudaStream_t st) {

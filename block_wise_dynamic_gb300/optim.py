@@ -7,6 +7,8 @@ class is that switch:
     from block_wise_dynamic_gb300 import Adam8bit
     opt = Adam8bit(model.parameters(), lr=1e-3, betas=(0.9, 0.999), eps=1e-8)
 
+``AdamW8bit`` is the same with decoupled weight decay.
+
 Parameters must be fp32 CUDA tensors (master weights); gradients fp32 or
 bf16.  Per parameter the state holds ``step`` and the codes and absmax of
 both moments; ``state_dict()`` / ``load_state_dict()`` round-trip them
@@ -24,6 +26,11 @@ from . import MultiTensorArgs, num_blocks, state_init
 
 
 class Adam8bit(torch.optim.Optimizer):
+    """8-bit Adam (``weight_decay`` must be 0: torch.optim.Adam's coupled L2
+    decay is not part of this step; use :class:`AdamW8bit` for decay)."""
+
+    _decoupled = False
+
     def __init__(self, params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.0):
         if lr < 0.0:
             raise ValueError(f"invalid learning rate {lr}")
@@ -31,8 +38,8 @@ class Adam8bit(torch.optim.Optimizer):
             raise ValueError(f"invalid betas {betas}")
         if eps < 0.0:
             raise ValueError(f"invalid eps {eps}")
-        if weight_decay != 0.0:
-            raise ValueError("weight_decay is not supported by this step")
+        if weight_decay < 0.0 or (weight_decay != 0.0 and not self._decoupled):
+            raise ValueError("Adam8bit takes no weight decay; AdamW8bit applies it decoupled")
         super().__init__(params, dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay))
         self._args_cache = {}
 
@@ -80,7 +87,8 @@ class Adam8bit(torch.optim.Optimizer):
                     self._args_cache[key] = (ptrs, args)
                 else:
                     args = cached[1]
-                args.step(lr=group["lr"], beta1=b1, beta2=b2, eps=group["eps"], step=t)
+                args.step(lr=group["lr"], beta1=b1, beta2=b2, eps=group["eps"],
+                          weight_decay=group["weight_decay"], step=t)
         return loss
 
     def load_state_dict(self, state_dict):
@@ -92,3 +100,13 @@ class Adam8bit(torch.optim.Optimizer):
             for k in ("m_codes", "v_codes"):
                 if k in st and st[k].dtype != torch.uint8:
                     st[k] = st[k].to(torch.uint8)
+
+
+class AdamW8bit(Adam8bit):
+    """8-bit AdamW: decoupled weight decay, p <- p * (1 - lr * weight_decay)
+    before the Adam update (torch.optim.AdamW's rule)."""
+
+    _decoupled = True
+
+    def __init__(self, params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=1e-2):
+        super().__init__(params, lr=lr, betas=betas, eps=eps, weight_decay=weight_decay)

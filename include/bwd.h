@@ -13,7 +13,7 @@
  * Conventions shared by every entry point
  *   - Pointers named "device" are CUDA device (or managed) memory of the
  *     CURRENT device; the caller owns them.  The library keeps only its own
- *     immutable code tables (about 9 KB per device, uploaded on first use).
+ *     immutable code tables (about 32 KB per device, uploaded on first use).
  *   - Every device operation is enqueued on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) and returns without waiting for it.  Launch
  *     errors are reported as BWD_ERR_CUDA; faults inside a kernel surface on
@@ -61,8 +61,9 @@ typedef enum {
 typedef enum { BWD_F32 = 0, BWD_BF16 = 1 } bwd_dtype;
 
 /* Adam hyper-parameters (section 一: first and second moment).  `step` is
- * the 1-based index t of the step being taken (bias corrections use it);
- * weight_decay must be 0. */
+ * the 1-based index t of the step being taken (bias corrections use it).
+ * weight_decay >= 0 is decoupled weight decay (AdamW, an extension of the
+ * method): p is first scaled by fp32(1 - lr * weight_decay); 0 gives Adam. */
 typedef struct {
   float lr;
   float beta1;
@@ -118,15 +119,19 @@ bwd_status bwd_state_init(uint8_t* m_codes, float* m_absmax, uint8_t* v_codes,
 /* One 8-bit Adam step on one flat tensor (section 二, opening paragraph):
  * dequantize m (signed map) and v (unsigned map), run Adam in fp32,
  *     m = b1 m + (1-b1) g;  v = b2 v + ((1-b2) g) g;
- *     p = p - (s m) / (sqrt(v) / c + eps),
- * with s = fp32(lr / (1 - b1^t)) and c = fp32(sqrt(1 - b2^t)) formed in
- * binary64 on the host, each element operation one binary32 rounding in
- * that order; then requantize m and v block by block with fresh absmax.
+ *     p = p d - (s m) / (sqrt(v) / c + eps),
+ * with s = fp32(lr / (1 - b1^t)), c = fp32(sqrt(1 - b2^t)) and the decay
+ * factor d = fp32(1 - lr wd) formed in binary64 on the host; then requantize
+ * m and v block by block with fresh absmax.  m and v take one binary32
+ * rounding per operation in that order, so the new codes and absmax are
+ * exactly those of IEEE arithmetic; the parameter update uses approximate
+ * (rsqrt / rcp) arithmetic and is within a few ulps of the update term.
  *   p                : device float[n], updated in place.
  *   g                : device, float[n] or bf16[n] per g_dtype, read only.
  *   m_codes, v_codes : device uint8[n], updated in place.
  *   m_absmax,v_absmax: device float[ceil(n/2048)], updated in place.
- *   hp               : host pointer; hp->step >= 1, weight_decay == 0. */
+ *   hp               : host pointer; hp->step >= 1, lr and eps finite,
+ *                      eps >= 0, betas in [0, 1), weight_decay finite >= 0. */
 bwd_status bwd_adam8bit_step(float* p, const void* g, bwd_dtype g_dtype,
                              uint8_t* m_codes, float* m_absmax,
                              uint8_t* v_codes, float* v_absmax, int64_t n,

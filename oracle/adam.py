@@ -26,8 +26,14 @@ Readings where the page is silent:
   t counts from 1; the state before step 1 is all codes of +0.0 with absmax 0
   (R6), which dequantizes to exact zeros.  bf16 gradients widen exactly.
 
-Parity: ``adam_update_fp32`` is pinned against ``torch.optim.Adam`` on the CPU
-(tests/test_oracle_adam.py) and against the closed form of Adam's first step;
+Decoupled weight decay (AdamW; not on the page, the first extension of the
+method): with weight_decay wd > 0 the parameters are first scaled,
+p = p * f32(1 - lr * wd) (factor formed in binary64), then updated as above
+with the same moments.  wd = 0 gives a factor of exactly 1.
+
+Parity: ``adam_update_fp32`` is pinned against ``torch.optim.Adam`` and
+``torch.optim.AdamW`` on the CPU (tests/test_oracle_adam.py) and against the
+closed forms of Adam's first step and of a pure decay step;
 the 8-bit step is pinned by its quantization invariants and by a trajectory
 band around 32-bit Adam.
 """
@@ -64,6 +70,7 @@ def host_scalars(hp: AdamHParams):
     if hp.step < 1:
         raise ValueError("step counts from 1")
     lr, b1, b2, _ = (float(v) for v in hp.f32())
+    wd = float(F32(hp.weight_decay))
     bc1 = 1.0 - b1 ** hp.step
     bc2 = 1.0 - b2 ** hp.step
     return {
@@ -71,6 +78,7 @@ def host_scalars(hp: AdamHParams):
         "bc2_sqrt": F32(math.sqrt(bc2)),
         "one_minus_beta1": F32(1.0 - b1),
         "one_minus_beta2": F32(1.0 - b2),
+        "decay": F32(1.0 - lr * wd),
     }
 
 
@@ -81,9 +89,9 @@ def widen_bf16(bits) -> np.ndarray:
 
 
 def adam_update_fp32(p, g, m_old, v_old, hp: AdamHParams):
-    """One binary32 Adam update (R10).  Returns new (p, m, v); inputs unchanged."""
-    if hp.weight_decay != 0.0:
-        raise NotImplementedError("weight decay is not part of this step")
+    """One binary32 Adam(W) update (R10).  Returns new (p, m, v); inputs unchanged."""
+    if hp.weight_decay < 0.0:
+        raise ValueError("weight decay must be >= 0")
     p = np.asarray(p, F32)
     g = np.asarray(g, F32)
     m_old = np.asarray(m_old, F32)
@@ -93,7 +101,7 @@ def adam_update_fp32(p, g, m_old, v_old, hp: AdamHParams):
     m = b1 * m_old + s["one_minus_beta1"] * g
     v = b2 * v_old + (s["one_minus_beta2"] * g) * g
     denom = np.sqrt(v) / s["bc2_sqrt"] + eps
-    p_new = p - (s["step_size"] * m) / denom
+    p_new = (p * s["decay"]) - (s["step_size"] * m) / denom
     return p_new.astype(F32), m.astype(F32), v.astype(F32)
 
 

@@ -94,7 +94,8 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
                 AdamHParams(1e-3, 0.9, -0.1, 1e-8, 0.0, 1),       # beta2 < 0
                 AdamHParams(float("nan"), 0.9, 0.999, 1e-8, 0.0, 1),
                 AdamHParams(1e-3, 0.9, 0.999, -1.0, 0.0, 1),      # eps < 0
-                AdamHParams(1e-3, 0.9, 0.999, 1e-8, 0.01, 1)):    # weight decay
+                AdamHParams(1e-3, 0.9, 0.999, 1e-8, -0.01, 1),    # negative weight decay
+                AdamHParams(1e-3, 0.9, 0.999, 1e-8, float("inf"), 1)):
         assert step(fake, fake, 0, fake, fake, fake, fake, 10, ctypes.byref(bad), None) == 1
     assert step(None, fake, 0, fake, fake, fake, fake, 10, ctypes.byref(hp), None) == 1
 

@@ -272,3 +272,40 @@ def test_full_size_ragged_2000_sampled(bwd):
 
 def test_full_size_gpt_350m_flat_sampled(bwd):
     assert _sampled_full_size(bwd, W.workload("gpt_350m"), blocks_per_tensor=200) > 100
+
+
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
+def test_adamw_single_step_from_identical_state(bwd, gdt):
+    """Decoupled weight decay: p is scaled by 1 - lr*wd before the update."""
+    n = 3 * B + 333
+    p = W.gen_normal(n, 0.02, seed=77).numpy()
+    g = W.gen_normal(n, 1e-2, seed=78, dtype=gdt)
+    st = random_state(n, 79)
+    for wd in (0.01, 0.2):
+        hp = oracle.AdamHParams(lr=3e-3, weight_decay=wd, step=5)
+        tp, tmc, tma, tvc, tva = to_dev(p, *st)
+        bwd.adam8bit_step(tp, g.to(DEV), tmc, tma, tvc, tva, lr=hp.lr, weight_decay=wd, step=hp.step)
+        torch.cuda.synchronize()
+        got = tuple(t.cpu().numpy() for t in (tp, tmc, tma, tvc, tva))
+        compare_step(got, oracle.adam8bit_step(p, g_to_np(g), *st, hp))
+
+
+def test_adamw8bit_optimizer_matches_oracle(bwd):
+    torch.manual_seed(1)
+    ps = [torch.nn.Parameter(torch.randn(n, device=DEV) * 0.02) for n in (5000, 2048 * 3, 17)]
+    ref = [(p.detach().cpu().numpy().copy(), *oracle.state_init(p.numel())) for p in ps]
+    opt = bwd.AdamW8bit(ps, lr=2e-3, weight_decay=0.1)
+    with pytest.raises(ValueError):
+        bwd.Adam8bit(ps, weight_decay=0.1)
+    for t in range(1, 5):
+        grads = [torch.randn(p.numel(), device=DEV) * 1e-2 for p in ps]
+        for p, g in zip(ps, grads):
+            p.grad = g
+        opt.step()
+        hp = oracle.AdamHParams(lr=2e-3, weight_decay=0.1, step=t)
+        ref = [oracle.adam8bit_step(r[0], g.cpu().numpy(), *r[1:], hp) for r, g in zip(ref, grads)]
+    for p, r in zip(ps, ref):
+        st = opt.state[p]
+        got = (p.detach().cpu().numpy(), st["m_codes"].cpu().numpy(), st["m_absmax"].cpu().numpy(),
+               st["v_codes"].cpu().numpy(), st["v_absmax"].cpu().numpy())
+        compare_step(got, r)

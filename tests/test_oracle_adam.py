@@ -158,3 +158,38 @@ def test_bf16_widening():
     vals = torch.tensor([1.0, -2.5, 3.140625, 1e-3, 0.0, -0.0], dtype=torch.bfloat16)
     bits = vals.view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(widen_bf16(bits), vals.float().numpy())
+
+
+@pytest.mark.parametrize("wd", [1e-2, 0.1])
+def test_fp32_update_matches_torch_adamw(wd):
+    """Decoupled weight decay: compare with torch.optim.AdamW over 20 steps."""
+    rng = np.random.default_rng(8)
+    n = 3001
+    p0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    hp0 = oracle.AdamHParams(lr=1e-3, weight_decay=wd)
+    lr32, b1, b2, e32 = (float(v) for v in hp0.f32())
+    tp = torch.nn.Parameter(torch.from_numpy(p0.copy()))
+    opt = torch.optim.AdamW([tp], lr=lr32, betas=(b1, b2), eps=e32, weight_decay=float(np.float32(wd)),
+                            foreach=False)
+    p, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    for t in range(1, 21):
+        g = (rng.standard_normal(n) * 10.0 ** rng.uniform(-4, 0, n)).astype(np.float32)
+        tp.grad = torch.from_numpy(g.copy())
+        opt.step()
+        p, m, v = oracle.adam_update_fp32(p, g, m, v, oracle.AdamHParams(lr=1e-3, weight_decay=wd, step=t))
+        pt = tp.detach().numpy()
+        np.testing.assert_allclose(p, pt, rtol=4e-6, atol=4e-7 * np.abs(pt).max())
+
+
+def test_decay_only_step_closed_form():
+    """Zero gradient and zero moments: the step only scales p by 1 - lr*wd."""
+    p = (np.random.default_rng(3).standard_normal(777) * 0.02).astype(np.float32)
+    z = np.zeros_like(p)
+    hp = oracle.AdamHParams(lr=2e-3, weight_decay=0.05, step=4)
+    p1, m, v = oracle.adam_update_fp32(p, z, z, z, hp)
+    assert np.all(m == 0) and np.all(v == 0)
+    factor = np.float32(1.0 - float(np.float32(2e-3)) * float(np.float32(0.05)))
+    assert np.array_equal(p1, (p * factor).astype(np.float32))
+    np.testing.assert_allclose(p1, p * (1 - 2e-3 * 0.05), rtol=1e-6)
+    with pytest.raises(ValueError):
+        oracle.adam_update_fp32(p, z, z, z, oracle.AdamHParams(weight_decay=-1.0))
