@@ -117,6 +117,8 @@ __device__ __forceinline__ uint32_t ld_stream_u1(const void* p) {
   return r;
 }
 
+
+
 // Code of a normalised value (see the count tables in tables.h).  The clamps
 // keep any bit pattern, non-finite ones included, inside the tables.
 __device__ __forceinline__ uint32_t code_signed(float q, const bwd::Tables& tab) {
@@ -148,7 +150,7 @@ __device__ __forceinline__ uint32_t code_unsigned(float q, const bwd::Tables& ta
 // redone with IEEE division.
 template <bool kSigned, bool kAnySign>
 __device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, const bwd::Tables& tab,
-                                           uint32_t (&w)[kQuads]) {
+                                               uint32_t (&w)[kQuads]) {
   uint32_t c[kPer];
   if (a == 0.0f) {
 #pragma unroll
@@ -158,10 +160,11 @@ __device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, 
     if (d.fast) {
       int minb = 0x7fffffff;
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const float q = bwd::div_fast(d, x[j]);
-        if (kSigned) minb = min(minb, __float_as_int(q));
-        c[j] = kSigned ? code_signed(q, tab) : (kAnySign ? code_unsigned(q, tab) : code_unsigned_nonneg(q, tab));
+      for (int j = 0; j < kPer; j += 2) {
+        const float2 q = bwd::div_fast2(d, make_float2(x[j], x[j + 1]));
+        if (kSigned) minb = min(minb, min(__float_as_int(q.x), __float_as_int(q.y)));
+        c[j] = kSigned ? code_signed(q.x, tab) : (kAnySign ? code_unsigned(q.x, tab) : code_unsigned_nonneg(q.x, tab));
+        c[j + 1] = kSigned ? code_signed(q.y, tab) : (kAnySign ? code_unsigned(q.y, tab) : code_unsigned_nonneg(q.y, tab));
       }
       if (kSigned && minb <= static_cast<int>(0x8E000000u)) {
 #pragma unroll
@@ -444,26 +447,36 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
       }
     }
 
-    // dequantize -> Adam in fp32.  The moments take one rounding per
-    // operation in the oracle's order, so they (and the codes and absmax
-    // derived from them) are bit-identical; the parameter update uses
-    // branch-free approximate sqrt and division (a few ulps of the update)
+    // dequantize -> Adam in fp32, two elements at a time.  The moments take
+    // one rounding per operation in the oracle's order, so they (and the
+    // codes and absmax derived from them) are bit-identical; the parameter
+    // update uses branch-free approximate sqrt and reciprocal (a few ulps
+    // of the update term)
     float m[kPer], v[kPer];
     float mx[2] = {0.0f, 0.0f};
+    const float2 ma2 = bwd::dup2(ma_old), va2 = bwd::dup2(va_old), tiny2 = bwd::dup2(1e-37f), ic2 = bwd::dup2(inv_bc2s);
+    const float2 eps2 = bwd::dup2(eps), nstep2 = bwd::dup2(-step_size), decay2 = bwd::dup2(decay);
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const float m_old = __fmul_rn(map_s[byte_of(mw[j >> 2], j & 3)], ma_old);
-      const float v_old = __fmul_rn(map_u[byte_of(vw[j >> 2], j & 3)], va_old);
-      const float gj = g[j];
-      m[j] = __fadd_rn(__fmul_rn(b1, m_old), __fmul_rn(omb1, gj));
-      v[j] = __fadd_rn(__fmul_rn(b2, v_old), __fmul_rn(__fmul_rn(omb2, gj), gj));
-      // sqrt(v) = v * rsqrt(v); the 1e-37 keeps rsqrt finite at v = 0 and
-      // does not change sqrt(v) / bc2s + eps for any v that matters
-      const float rs = rsqrt_approx(__fadd_rn(v[j], 1e-37f));
-      const float denom = __fmaf_rn(__fmul_rn(v[j], rs), inv_bc2s, eps);
-      p[j] = __fmaf_rn(-__fmul_rn(step_size, m[j]), rcp_approx(denom), __fmul_rn(p[j], decay));
-      mx[0] = fmaxf(mx[0], fabsf(m[j]));
-      mx[1] = fmaxf(mx[1], v[j]);
+    for (int j = 0; j < kPer; j += 2) {
+      const float2 mo = bwd::mul2(make_float2(map_s[byte_of(mw[j >> 2], j & 3)], map_s[byte_of(mw[j >> 2], (j & 3) + 1)]), ma2);
+      const float2 vo = bwd::mul2(make_float2(map_u[byte_of(vw[j >> 2], j & 3)], map_u[byte_of(vw[j >> 2], (j & 3) + 1)]), va2);
+      const float2 g2 = make_float2(g[j], g[j + 1]);
+      // the moments stay scalar: a packed multiply feeding a packed add may be
+      // contracted into one fused operation, which would change the rounding
+      const float2 mm = make_float2(__fadd_rn(__fmul_rn(b1, mo.x), __fmul_rn(omb1, g2.x)),
+                                    __fadd_rn(__fmul_rn(b1, mo.y), __fmul_rn(omb1, g2.y)));
+      const float2 vv = make_float2(__fadd_rn(__fmul_rn(b2, vo.x), __fmul_rn(__fmul_rn(omb2, g2.x), g2.x)),
+                                    __fadd_rn(__fmul_rn(b2, vo.y), __fmul_rn(__fmul_rn(omb2, g2.y), g2.y)));
+      m[j] = mm.x; m[j + 1] = mm.y; v[j] = vv.x; v[j + 1] = vv.y;
+      // sqrt(v) = v * rsqrt(v); the 1e-37 keeps rsqrt finite at v = 0
+      const float2 vt = bwd::add2(vv, tiny2);
+      const float2 rs = make_float2(rsqrt_approx(vt.x), rsqrt_approx(vt.y));
+      const float2 den = bwd::fma2(bwd::mul2(vv, rs), ic2, eps2);
+      const float2 rc = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+      const float2 pp = bwd::fma2(bwd::mul2(nstep2, mm), rc, bwd::mul2(make_float2(p[j], p[j + 1]), decay2));
+      p[j] = pp.x; p[j + 1] = pp.y;
+      mx[0] = fmaxf(mx[0], fmaxf(fabsf(mm.x), fabsf(mm.y)));
+      mx[1] = fmaxf(mx[1], fmaxf(vv.x, vv.y));
     }
     if (vec) {
 #pragma unroll

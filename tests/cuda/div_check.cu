@@ -1,4 +1,5 @@
-// Check of bwd::div_fast (exact_div.cuh) against __fdiv_rn, bit for bit.
+// Check of bwd::div_fast and the packed bwd::div_fast2 (exact_div.cuh)
+// against __fdiv_rn, bit for bit.
 // Usage: div_check [divisor_significands [first]]; all 2^23 divisor
 // significands (about 90 s on one GB300) make the check exhaustive over every
 // pair of binary32 significands and both signs of the dividend.
@@ -35,6 +36,12 @@ __global__ void part1(uint32_t a_lo) {
     if (__float_as_uint(q) != __float_as_uint(e)) { ++bad; record(x, a); }
     const float qn = bwd::div_fast(d, -x);
     if (__float_as_uint(qn) != (__float_as_uint(e) ^ 0x80000000u)) { ++bad; record(-x, a); }
+    // the packed routine, one lane each sign
+    const float2 q2 = bwd::div_fast2(d, make_float2(x, -x));
+    if (__float_as_uint(q2.x) != __float_as_uint(e) || __float_as_uint(q2.y) != (__float_as_uint(e) ^ 0x80000000u)) {
+      ++bad;
+      record(x, a);
+    }
   }
   atomicAdd(&g_bad, bad);
   atomicAdd(&g_checked, 2 * n);
@@ -62,8 +69,10 @@ __global__ void part2(uint32_t seed, uint32_t iters) {
     const bwd::Divisor d = bwd::make_divisor(a, 1);
     if (!d.fast) continue;
     const float q = bwd::div_fast(d, x);
+    const float2 q2 = bwd::div_fast2(d, make_float2(x, x));
     ++n;
-    if (__float_as_uint(q) != __float_as_uint(e)) { ++bad; record(x, a); }
+    if (__float_as_uint(q) != __float_as_uint(e) || __float_as_uint(q2.x) != __float_as_uint(e) ||
+        __float_as_uint(q2.y) != __float_as_uint(e)) { ++bad; record(x, a); }
   }
   atomicAdd(&g_bad, bad);
   atomicAdd(&g_checked, n);

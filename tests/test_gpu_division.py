@@ -1,6 +1,6 @@
-"""The per-block division used by the quantizers (exact_div.cuh: a correctly
-rounded reciprocal plus Markstein's correction) against the GPU's IEEE
-division, bit for bit.  The full run over all 2^23 divisor significands
+"""The per-block division used by the quantizers (exact_div.cuh, scalar and
+packed-pair forms: a correctly rounded reciprocal plus Markstein's
+correction) against the GPU's IEEE division, bit for bit.  The full run over all 2^23 divisor significands
 (about 90 s) is exhaustive; here the first and last 16,384 divisor
 significands (the last ones include the all-ones significand) are checked
 against every dividend significand of both signs, plus 1.6e10 random pairs
