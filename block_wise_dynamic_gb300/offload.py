@@ -32,7 +32,7 @@ class PipelinedHostStep:
     def __init__(self, dev_params: Sequence[torch.Tensor], dev_grads: Sequence[torch.Tensor],
                  m_codes, m_absmax, v_codes, v_absmax,
                  host_grads: Sequence[torch.Tensor], host_params: Sequence[torch.Tensor],
-                 chunk_bytes: int = 1 << 30):
+                 chunk_bytes: int = 256 << 20):
         T = len(dev_params)
         if not (len(dev_grads) == len(host_grads) == len(host_params) == T):
             raise ValueError("all lists must have the same length")
