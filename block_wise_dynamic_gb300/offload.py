@@ -59,7 +59,8 @@ class PipelinedHostStep:
             self.h2d = torch.cuda.Stream(self.device)
             self.d2h = torch.cuda.Stream(self.device)
 
-    def step(self, *, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, step, stream=None) -> None:
+    def step(self, *, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step,
+             stream=None) -> None:
         """Enqueue one step; the caller's stream (default: current) runs the
         kernels and, when it is done, the host parameters are complete."""
         if not self.chunks:
@@ -74,7 +75,8 @@ class PipelinedHostStep:
                 arrived = torch.cuda.Event()
                 arrived.record(self.h2d)
             comp.wait_event(arrived)
-            args.step(lr=lr, beta1=beta1, beta2=beta2, eps=eps, step=step, stream=comp)
+            args.step(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay, step=step,
+                      stream=comp)
             stepped = torch.cuda.Event()
             stepped.record(comp)
             self.d2h.wait_event(stepped)

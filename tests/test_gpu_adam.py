@@ -309,3 +309,32 @@ def test_adamw8bit_optimizer_matches_oracle(bwd):
         got = (p.detach().cpu().numpy(), st["m_codes"].cpu().numpy(), st["m_absmax"].cpu().numpy(),
                st["v_codes"].cpu().numpy(), st["v_absmax"].cpu().numpy())
         compare_step(got, r)
+
+
+def test_step_on_tensor_larger_than_2p31_elements(bwd):
+    """64-bit indexing in the fused step: one tensor of 2^31 + 5 parameters;
+    blocks at the 2^31 boundary and the ragged tail against the oracle."""
+    n = (1 << 31) + 5
+    p = torch.empty(n, dtype=torch.float32, device=DEV)
+    p.normal_(0.0, 0.02, generator=torch.Generator(device=DEV).manual_seed(1))
+    g = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    g.normal_(0.0, 1e-3, generator=torch.Generator(device=DEV).manual_seed(2))
+    mc, ma, vc, va = bwd.state_init(n, DEV)
+    bwd.adam8bit_step(p, g, mc, ma, vc, va, lr=1e-3, step=1)
+    picks = [0, (1 << 31) // B - 1, (1 << 31) // B]
+    saved = {}
+    for b in picks:
+        lo, hi = b * B, min(n, (b + 1) * B)
+        saved[b] = (p[lo:hi].cpu().numpy(), g_to_np(g[lo:hi]), mc[lo:hi].cpu().numpy(), ma[b:b + 1].cpu().numpy(),
+                    vc[lo:hi].cpu().numpy(), va[b:b + 1].cpu().numpy())
+    bwd.adam8bit_step(p, g, mc, ma, vc, va, lr=1e-3, step=2)
+    torch.cuda.synchronize()
+    hp = oracle.AdamHParams(lr=1e-3, step=2)
+    for b in picks:
+        lo, hi = b * B, min(n, (b + 1) * B)
+        ref = oracle.adam8bit_step(*saved[b], hp)
+        got = (p[lo:hi].cpu().numpy(), mc[lo:hi].cpu().numpy(), ma[b:b + 1].cpu().numpy(),
+               vc[lo:hi].cpu().numpy(), va[b:b + 1].cpu().numpy())
+        compare_step(got, ref)
+    del p, g, mc, ma, vc, va
+    torch.cuda.empty_cache()

@@ -166,3 +166,66 @@ def test_full_size_2p28_sampled(bwd):
         del c, a, y, xs
     del x
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("signed", [True, False])
+def test_extreme_block_scales(bwd, signed):
+    """Blocks whose absmax is subnormal, tiny, or close to FLT_MAX (the
+    divisor takes IEEE division there) and blocks mixing a huge absmax with
+    subnormal values, all bit-exact."""
+    rng = np.random.default_rng(21)
+    B = 2048
+    scales = [1e-44, 1e-40, 3e-38, 1e-30, 1.0, 1e30, 1e37, 5e37]  # |x| stays finite
+    rows = []
+    for s in scales:
+        r = (rng.standard_normal(B) * np.float32(s)).astype(np.float32)
+        rows.append(r)
+    mixed = (rng.standard_normal(B) * 1e-42).astype(np.float32)
+    mixed[7] = np.float32(3.0e38)
+    rows.append(mixed)
+    neg_tiny = -np.abs(rng.standard_normal(B) * 1e-44).astype(np.float32)
+    neg_tiny[3] = np.float32(2.5)  # -> tiny negative quotients, -0.0 vs negative subnormal
+    rows.append(neg_tiny)
+    x = np.concatenate(rows)
+    if not signed:
+        x = np.abs(x)
+    c, a = gpu_quant(bwd, x, signed)
+    co, ao = oracle.quantize_blockwise(x, signed)
+    assert np.array_equal(a.view(U32), ao.view(U32))
+    assert np.array_equal(c, co)
+
+
+def test_non_finite_inputs_do_not_fault(bwd):
+    """Outside the method, but they must not fault or touch other blocks."""
+    B = 2048
+    x = W.quant_input(4 * B, seed=5).numpy()
+    x[10] = np.nan
+    x[B + 3] = np.inf
+    x[2 * B + 1] = -np.inf
+    for signed in (True, False):
+        c, a = gpu_quant(bwd, x, signed)
+        co, ao = oracle.quantize_blockwise(x[3 * B:], signed)
+        assert np.array_equal(c[3 * B:], co) and a[3] == ao[0]
+
+
+def test_tensor_larger_than_2p31_elements(bwd):
+    """64-bit indexing: one tensor of 2^31 + 2049 elements; the blocks at the
+    2^31 boundary and the ragged tail are checked against the oracle."""
+    B = 2048
+    n = (1 << 31) + 2049
+    x = torch.empty(n, dtype=torch.float32, device=DEV)
+    x.normal_(0.0, 1.0, generator=torch.Generator(device=DEV).manual_seed(3))
+    c, a = bwd.quantize_blockwise(x, "signed")
+    y = bwd.dequantize_blockwise(c, a, "signed")
+    torch.cuda.synchronize()
+    nb = (n + B - 1) // B
+    for b in (0, (1 << 31) // B - 1, (1 << 31) // B, nb - 1):
+        lo, hi = b * B, min(n, (b + 1) * B)
+        xb = x[lo:hi].cpu().numpy()
+        co, ao = oracle.quantize_blockwise(xb, True)
+        assert np.array_equal(c[lo:hi].cpu().numpy(), co)
+        assert a[b].item() == ao[0]
+        yo = oracle.dequantize_blockwise(co, ao, True)
+        assert np.array_equal(y[lo:hi].cpu().numpy().view(U32), yo.view(U32))
+    del x, c, a, y
+    torch.cuda.empty_cache()
