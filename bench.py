@@ -37,10 +37,11 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 126 * 2 ** 20
 
 
-def algorithmic_bytes_per_param(grad_bytes: int) -> float:
-    """p read+write 8, g read, m and v codes read+write 2 + 2, and the two
-    fp32 absmax per 2048 block read+write (16 B / 2048)."""
-    return 8 + grad_bytes + 4 + 16.0 / 2048
+def algorithmic_bytes_per_param(grad_bytes: int, param_bytes: int = 4) -> float:
+    """p read+write (8 for fp32, 4 for bf16), g read, m and v codes
+    read+write 2 + 2, and the two fp32 absmax per 2048 block read+write
+    (16 B / 2048)."""
+    return 2 * param_bytes + grad_bytes + 4 + 16.0 / 2048
 
 
 def parse_args():
@@ -51,6 +52,8 @@ def parse_args():
     ap.add_argument("--workload", default="llama2_7b",
                     choices=["llama2_7b", "gpt_350m", "ragged_2000", "adam_1m", "quant_2p28"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--param-dtype", default="f32", choices=["f32", "bf16"],
+                    help="parameter storage (bf16: widened for the update, rounded back)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -267,11 +270,13 @@ def run_ours(args):
     sizes = [n for n in wl.sizes if n > 0]
     N = sum(sizes)
     gbytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
-    bpp = algorithmic_bytes_per_param(gbytes)
+    pdtype = torch.bfloat16 if args.param_dtype == "bf16" else torch.float32
+    pbytes = 2 if pdtype == torch.bfloat16 else 4
+    bpp = algorithmic_bytes_per_param(gbytes, pbytes)
 
     ps, gs, sts = [], [], []
     for i, n in enumerate(sizes):
-        ps.append(W.gen_normal(n, 0.02, seed=rank * 1_000_003 + i, device=dev))
+        ps.append(W.gen_normal(n, 0.02, seed=rank * 1_000_003 + i, device=dev, dtype=pdtype))
         gs.append(W.gen_normal(n, wl.grad_std[i], seed=rank * 1_000_003 + 500_000 + i, device=dev,
                                dtype=wl.grad_dtype))
         sts.append(bwd.state_init(n, dev))
@@ -316,15 +321,15 @@ def run_ours(args):
     # gradients arrive from pinned host memory and the updated parameters go
     # back to it, copies inside the timed region
     e2e = None
-    pinned_bytes = N * (gbytes + 4)
+    pinned_bytes = N * (gbytes + pbytes)
     if args.e2e_steps > 0 and host_mem_available() < 2 * pinned_bytes * max(world, 1):
-        e2e = {"value": None, "unit": "params/s", "h2d_bytes_per_step": N * gbytes, "d2h_bytes_per_step": N * 4,
+        e2e = {"value": None, "unit": "params/s", "h2d_bytes_per_step": N * gbytes, "d2h_bytes_per_step": N * pbytes,
                "skipped": f"needs {pinned_bytes / 1e9:.0f} GB of pinned host memory per rank"}
     elif args.e2e_steps > 0:
         from block_wise_dynamic_gb300.offload import PipelinedHostStep
 
         gh = torch.empty(N, dtype=wl.grad_dtype, pin_memory=True)
-        ph = torch.empty(N, dtype=torch.float32, pin_memory=True)
+        ph = torch.empty(N, dtype=pdtype, pin_memory=True)
         off = 0
         ghv, phv = [], []
         for i, n in enumerate(sizes):
@@ -350,7 +355,7 @@ def run_ours(args):
         e2e_ms = f0.elapsed_time(f1)
         e2e_ms = max_over_ranks(e2e_ms, dev)
         e2e = {"value": world * N * args.e2e_steps / (e2e_ms / 1e3), "unit": "params/s",
-               "h2d_bytes_per_step": N * gbytes, "d2h_bytes_per_step": N * 4,
+               "h2d_bytes_per_step": N * gbytes, "d2h_bytes_per_step": N * pbytes,
                "steps": args.e2e_steps,
                "what": "per step through block_wise_dynamic_gb300.offload.PipelinedHostStep: gradients "
                        "H2D from pinned host memory, the 8-bit step, updated fp32 parameters D2H into "
@@ -386,6 +391,7 @@ def run_ours(args):
             "params": N,
             "tensors": len(sizes),
             "grad_dtype": "bf16" if gbytes == 2 else "f32",
+            "param_dtype": args.param_dtype,
             "state": "u8 codes (signed m, unsigned v) + f32 absmax per 2048 block",
             "l2": f"inputs larger than L2 ({bpp * N / 1e9:.1f} GB per step vs {L2_BYTES / 2**20:.0f} MiB L2), no flush",
             "parallelism": f"replica per GPU x{world}",
@@ -393,13 +399,13 @@ def run_ours(args):
         "hbm_gbs": bpp * N / (elapsed_ms / args.steps / 1e3) / 1e9,
         "roofline": {
             "bound": "hbm",
-            "kernel": "adam8bit_kernel<bf16>" if gbytes == 2 else "adam8bit_kernel<f32>",
+            "kernel": f"adam8bit_kernel<g {'bf16' if gbytes == 2 else 'f32'}, p {args.param_dtype}>",
             "achieved": achieved,
             "peak": peak,
             "peak_kind": f"{peak_kind} (copy bandwidth)",
             "unit": "GB/s",
             "frac": achieved / peak,
-            "traffic": None if tpp is None else tpp * N / launches_per_step,
+            "traffic": None if (tpp is None or pbytes != 4) else tpp * N / launches_per_step,
             "bytes_per_param": bpp,
             "mean_launch_ms": mean_launch_ms,
         },

@@ -154,7 +154,11 @@ def _hparams(lr, beta1, beta2, eps, step, weight_decay=0.0) -> _abi.AdamHParams:
 def adam8bit_step(p, g, m_codes, m_absmax, v_codes, v_absmax, *, lr=1e-3, beta1=0.9, beta2=0.999,
                   eps=1e-8, weight_decay=0.0, step, stream=None) -> None:
     """One 8-bit Adam step on one flat tensor, in place (``bwd_adam8bit_step``);
-    ``weight_decay`` > 0 makes it AdamW (decoupled)."""
+    ``weight_decay`` > 0 makes it AdamW (decoupled).  bf16 parameters go
+    through ``bwd_adam8bit_step_multi_ex``."""
+    if isinstance(p, torch.Tensor) and p.dtype == torch.bfloat16:
+        return adam8bit_step_multi([p], [g], [m_codes], [m_absmax], [v_codes], [v_absmax], lr=lr, beta1=beta1,
+                                   beta2=beta2, eps=eps, weight_decay=weight_decay, step=step, stream=stream)
     n = p.numel()
     _need(p, "p", torch.float32)
     if g.dtype not in _GDT:
@@ -184,13 +188,17 @@ class MultiTensorArgs:
         if not (len(grads) == len(m_codes) == len(m_absmax) == len(v_codes) == len(v_absmax) == T):
             raise ValueError("all lists must have the same length")
         gdt = {g.dtype for g in grads}
-        if len(gdt) > 1:
-            raise TypeError("all gradients of one call must share a dtype")
+        pdt = {p.dtype for p in params}
+        if len(gdt) > 1 or len(pdt) > 1:
+            raise TypeError("all gradients (and all parameters) of one call must share a dtype")
         self.g_dtype = _GDT[gdt.pop()] if T else _abi.BWD_F32
+        self.p_dtype = _GDT[pdt.pop()] if T else _abi.BWD_F32
         self.device = params[0].device if T else None
         for i in range(T):
             n = params[i].numel()
-            _need(params[i], f"params[{i}]", torch.float32)
+            _need(params[i], f"params[{i}]", params[i].dtype)
+            if params[i].dtype not in _GDT:
+                raise TypeError("parameters must be float32 or bfloat16")
             _need(grads[i], f"grads[{i}]", grads[i].dtype, n)
             _need(m_codes[i], f"m_codes[{i}]", torch.uint8, n)
             _need(v_codes[i], f"v_codes[{i}]", torch.uint8, n)
@@ -214,16 +222,17 @@ class MultiTensorArgs:
             return
         hp = _hparams(lr, beta1, beta2, eps, step, weight_decay)
         with torch.cuda.device(self.device):
-            st = _lib.bwd_adam8bit_step_multi(
-                self.T, self.p, self.g, self.g_dtype, self.mc, self.ma, self.vc, self.va, self.n,
-                ctypes.byref(hp), _stream_handle(self.device, stream),
+            st = _lib.bwd_adam8bit_step_multi_ex(
+                self.T, self.p, self.p_dtype, self.g, self.g_dtype, self.mc, self.ma, self.vc, self.va,
+                self.n, ctypes.byref(hp), _stream_handle(self.device, stream),
             )
-        _abi.check(st, "bwd_adam8bit_step_multi")
+        _abi.check(st, "bwd_adam8bit_step_multi_ex")
 
 
 def adam8bit_step_multi(params, grads, m_codes, m_absmax, v_codes, v_absmax, *, lr=1e-3, beta1=0.9,
                         beta2=0.999, eps=1e-8, weight_decay=0.0, step, stream=None) -> None:
-    """One 8-bit Adam(W) step over a list of tensors (``bwd_adam8bit_step_multi``)."""
+    """One 8-bit Adam(W) step over a list of tensors (``bwd_adam8bit_step_multi_ex``);
+    parameters fp32 or bf16, gradients fp32 or bf16."""
     MultiTensorArgs(params, grads, m_codes, m_absmax, v_codes, v_absmax).step(
         lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay, step=step, stream=stream
     )

@@ -60,6 +60,10 @@ _SIGNATURES = {
         _int,
         [_i32, _pp, _pp, _int, _pp, _pp, _pp, _pp, ctypes.POINTER(_i64), ctypes.POINTER(AdamHParams), _vp],
     ),
+    "bwd_adam8bit_step_multi_ex": (
+        _int,
+        [_i32, _pp, _int, _pp, _int, _pp, _pp, _pp, _pp, ctypes.POINTER(_i64), ctypes.POINTER(AdamHParams), _vp],
+    ),
     "bwd_status_string": (ctypes.c_char_p, [_int]),
     "bwd_last_error": (ctypes.c_char_p, []),
 }

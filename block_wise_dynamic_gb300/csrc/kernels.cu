@@ -27,6 +27,7 @@
 // and a negative subnormal give different codes, fall back to div.rn) and
 // the threshold compare.  The Adam update uses the same operations, in the
 // same order, as the CPU oracle.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -321,7 +322,7 @@ __global__ void fill_kernel(uint8_t* __restrict__ a, uint8_t va, uint8_t* __rest
 // 8-bit Adam
 
 struct TensorArgs {
-  float* p;
+  void* p;  // fp32 or bf16 parameters (kernel template argument)
   const void* g;
   uint8_t* mc;
   float* ma;
@@ -369,13 +370,21 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return r;
 }
 
+// One fp32 or bf16 element, widened to fp32 (bf16 widening is exact).
 template <bool kBf16>
 __device__ __forceinline__ float load_grad1(const void* g, int64_t i) {
   if (kBf16) return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(g)[i]) << 16);
   return static_cast<const float*>(g)[i];
 }
 
-template <bool kBf16>
+// bf16 bits of x, round to nearest even (CUDA's conversion).
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
+}
+
+// kBf16: gradient type; kPBf16: parameter type (bf16 parameters are widened
+// for the update and rounded back to bf16 on store).
+template <bool kBf16, bool kPBf16>
 __global__ void __launch_bounds__(kCta, 3)
 adam8bit_kernel(const __grid_constant__ AdamArgs args) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -421,8 +430,7 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
 #pragma unroll
       for (int k = 0; k < kQuads; ++k) {
         const int64_t e = base + kSpan * k + 4 * t;
-        const float4 a = ld_stream_f4(T.p + e);
-        p[4 * k] = a.x; p[4 * k + 1] = a.y; p[4 * k + 2] = a.z; p[4 * k + 3] = a.w;
+        load_grad4<kPBf16>(T.p, e, &p[4 * k]);
         load_grad4<kBf16>(T.g, e, &g[4 * k]);
         mw[k] = ld_stream_u1(T.mc + e);
         vw[k] = ld_stream_u1(T.vc + e);
@@ -437,7 +445,7 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
         for (int j = 0; j < 4; ++j) {
           const int e = slot(t, 4 * k + j);
           const bool in = e < rem;
-          p[4 * k + j] = in ? T.p[base + e] : 0.0f;
+          p[4 * k + j] = in ? load_grad1<kPBf16>(T.p, base + e) : 0.0f;
           g[4 * k + j] = in ? load_grad1<kBf16>(T.g, base + e) : 0.0f;
           cm[j] = in ? T.mc[base + e] : 128u;
           cv[j] = in ? T.vc[base + e] : 0u;
@@ -480,14 +488,24 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
     }
     if (vec) {
 #pragma unroll
-      for (int k = 0; k < kQuads; ++k)
-        __stcs(reinterpret_cast<float4*>(T.p + base + kSpan * k + 4 * t),
-               make_float4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]));
+      for (int k = 0; k < kQuads; ++k) {
+        const int64_t e = base + kSpan * k + 4 * t;
+        if (kPBf16)
+          __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(T.p) + e),
+                 make_uint2(bf16_bits(p[4 * k]) | (bf16_bits(p[4 * k + 1]) << 16),
+                            bf16_bits(p[4 * k + 2]) | (bf16_bits(p[4 * k + 3]) << 16)));
+        else
+          __stcs(reinterpret_cast<float4*>(static_cast<float*>(T.p) + e),
+                 make_float4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]));
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
         const int e = slot(t, j);
-        if (e < rem) T.p[base + e] = p[j];
+        if (e < rem) {
+          if (kPBf16) static_cast<uint16_t*>(T.p)[base + e] = static_cast<uint16_t>(bf16_bits(p[j]));
+          else static_cast<float*>(T.p)[base + e] = p[j];
+        }
       }
     }
 
@@ -541,7 +559,7 @@ struct DeviceState {
   int num_sms = 0;
   int occ_quant[2] = {0, 0};
   int occ_dequant[2] = {0, 0};
-  int occ_adam[2] = {0, 0};
+  int occ_adam[4] = {0, 0, 0, 0};  // [2 * parameter bf16 + gradient bf16]
 };
 
 std::mutex g_mu;
@@ -588,13 +606,16 @@ bwd_status ensure_device(DeviceState** out) {
                        reinterpret_cast<const void*>(quantize_kernel<false>)};
   const void* kd[2] = {reinterpret_cast<const void*>(dequantize_kernel<true>),
                        reinterpret_cast<const void*>(dequantize_kernel<false>)};
-  const void* ka[2] = {reinterpret_cast<const void*>(adam8bit_kernel<false>),
-                       reinterpret_cast<const void*>(adam8bit_kernel<true>)};
+  const void* ka[4] = {reinterpret_cast<const void*>(adam8bit_kernel<false, false>),
+                       reinterpret_cast<const void*>(adam8bit_kernel<true, false>),
+                       reinterpret_cast<const void*>(adam8bit_kernel<false, true>),
+                       reinterpret_cast<const void*>(adam8bit_kernel<true, true>)};
   for (int k = 0; k < 2; ++k) {
     if ((s = occupancy(kq[k], kQCta, kTablesBytes, &d.occ_quant[k])) != BWD_OK) return s;
     if ((s = occupancy(kd[k], kDeqThreads, 0, &d.occ_dequant[k])) != BWD_OK) return s;
-    if ((s = occupancy(ka[k], kCta, kTablesBytes, &d.occ_adam[k])) != BWD_OK) return s;
   }
+  for (int k = 0; k < 4; ++k)
+    if ((s = occupancy(ka[k], kCta, kTablesBytes, &d.occ_adam[k])) != BWD_OK) return s;
   d.ready = true;
   *out = &d;
   return BWD_OK;
@@ -645,12 +666,18 @@ void fill_scalars(const bwd_adam_hparams* hp, AdamArgs* a) {
   a->decay = static_cast<float>(1.0 - static_cast<double>(hp->lr) * static_cast<double>(hp->weight_decay));
 }
 
-bwd_status launch_adam_chunk(const AdamArgs& a, bool bf16, const DeviceState& d, cudaStream_t st) {
+bwd_status launch_adam_chunk(const AdamArgs& a, bool g_bf16, bool p_bf16, const DeviceState& d,
+                             cudaStream_t st) {
   const int64_t total = a.block_start[a.num_tensors];
   if (total == 0) return BWD_OK;
-  const int grid = grid_for(total, kGroups, d, d.occ_adam[bf16 ? 1 : 0]);
-  if (bf16) adam8bit_kernel<true><<<grid, kCta, kTablesBytes, st>>>(a);
-  else adam8bit_kernel<false><<<grid, kCta, kTablesBytes, st>>>(a);
+  const int grid = grid_for(total, kGroups, d, d.occ_adam[2 * p_bf16 + g_bf16]);
+  if (p_bf16) {
+    if (g_bf16) adam8bit_kernel<true, true><<<grid, kCta, kTablesBytes, st>>>(a);
+    else adam8bit_kernel<false, true><<<grid, kCta, kTablesBytes, st>>>(a);
+  } else {
+    if (g_bf16) adam8bit_kernel<true, false><<<grid, kCta, kTablesBytes, st>>>(a);
+    else adam8bit_kernel<false, false><<<grid, kCta, kTablesBytes, st>>>(a);
+  }
   return check_launch("adam8bit_kernel launch");
 }
 
@@ -735,13 +762,21 @@ bwd_status bwd_state_init(uint8_t* m_codes, float* m_absmax, uint8_t* v_codes, f
   return check_launch("fill_kernel launch");
 }
 
-bwd_status bwd_adam8bit_step_multi(int32_t num_tensors, float* const* p, const void* const* g,
-                                   bwd_dtype g_dtype, uint8_t* const* m_codes, float* const* m_absmax,
-                                   uint8_t* const* v_codes, float* const* v_absmax, const int64_t* n,
-                                   const bwd_adam_hparams* hp, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of the multi-tensor entry points; PP is float* const* or
+// void* const* (the parameter pointers).
+template <typename PP>
+bwd_status step_multi(int32_t num_tensors, PP p, bwd_dtype p_dtype, const void* const* g, bwd_dtype g_dtype,
+                      uint8_t* const* m_codes, float* const* m_absmax, uint8_t* const* v_codes,
+                      float* const* v_absmax, const int64_t* n, const bwd_adam_hparams* hp, void* stream) {
   if (num_tensors < 0) return fail(BWD_ERR_INVALID_ARG, "num_tensors < 0");
   if (g_dtype != BWD_F32 && g_dtype != BWD_BF16)
     return fail(BWD_ERR_UNSUPPORTED_DTYPE, "gradient dtype %d", (int)g_dtype);
+  if (p_dtype != BWD_F32 && p_dtype != BWD_BF16)
+    return fail(BWD_ERR_UNSUPPORTED_DTYPE, "parameter dtype %d", (int)p_dtype);
   bwd_status s = check_hparams(hp);
   if (s != BWD_OK) return s;
   if (num_tensors == 0) return BWD_OK;
@@ -760,7 +795,7 @@ bwd_status bwd_adam8bit_step_multi(int32_t num_tensors, float* const* p, const v
 
   static thread_local AdamArgs a;  // ~32 KB: kept off the stack
   fill_scalars(hp, &a);
-  const bool bf16 = g_dtype == BWD_BF16;
+  const bool g_bf16 = g_dtype == BWD_BF16, p_bf16 = p_dtype == BWD_BF16;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int k = 0;
   a.block_start[0] = 0;
@@ -779,16 +814,35 @@ bwd_status bwd_adam8bit_step_multi(int32_t num_tensors, float* const* p, const v
     ++k;
     if (k == kMaxTensors) {
       a.num_tensors = k;
-      if ((s = launch_adam_chunk(a, bf16, *d, st)) != BWD_OK) return s;
+      if ((s = launch_adam_chunk(a, g_bf16, p_bf16, *d, st)) != BWD_OK) return s;
       k = 0;
       a.block_start[0] = 0;
     }
   }
   if (k > 0) {
     a.num_tensors = k;
-    if ((s = launch_adam_chunk(a, bf16, *d, st)) != BWD_OK) return s;
+    if ((s = launch_adam_chunk(a, g_bf16, p_bf16, *d, st)) != BWD_OK) return s;
   }
   return BWD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+bwd_status bwd_adam8bit_step_multi(int32_t num_tensors, float* const* p, const void* const* g,
+                                   bwd_dtype g_dtype, uint8_t* const* m_codes, float* const* m_absmax,
+                                   uint8_t* const* v_codes, float* const* v_absmax, const int64_t* n,
+                                   const bwd_adam_hparams* hp, void* stream) {
+  return step_multi(num_tensors, p, BWD_F32, g, g_dtype, m_codes, m_absmax, v_codes, v_absmax, n, hp, stream);
+}
+
+bwd_status bwd_adam8bit_step_multi_ex(int32_t num_tensors, void* const* p, bwd_dtype p_dtype,
+                                      const void* const* g, bwd_dtype g_dtype, uint8_t* const* m_codes,
+                                      float* const* m_absmax, uint8_t* const* v_codes,
+                                      float* const* v_absmax, const int64_t* n,
+                                      const bwd_adam_hparams* hp, void* stream) {
+  return step_multi(num_tensors, p, p_dtype, g, g_dtype, m_codes, m_absmax, v_codes, v_absmax, n, hp, stream);
 }
 
 bwd_status bwd_adam8bit_step(float* p, const void* g, bwd_dtype g_dtype, uint8_t* m_codes,

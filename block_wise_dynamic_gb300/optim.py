@@ -9,8 +9,8 @@ class is that switch:
 
 ``AdamW8bit`` is the same with decoupled weight decay.
 
-Parameters must be fp32 CUDA tensors (master weights); gradients fp32 or
-bf16.  Per parameter the state holds ``step`` and the codes and absmax of
+Parameters are fp32 (master weights) or bf16 CUDA tensors (widened for the
+update, stored back rounded to nearest even); gradients fp32 or bf16.  Per parameter the state holds ``step`` and the codes and absmax of
 both moments; ``state_dict()`` / ``load_state_dict()`` round-trip them
 exactly.  Each ``step()`` issues one multi-tensor launch per (device,
 gradient dtype, step count) group.
@@ -62,20 +62,20 @@ class Adam8bit(torch.optim.Optimizer):
             for p in group["params"]:
                 if p.grad is None:
                     continue
-                if p.dtype != torch.float32 or not p.is_cuda:
-                    raise TypeError("Adam8bit needs fp32 CUDA parameters")
+                if p.dtype not in (torch.float32, torch.bfloat16) or not p.is_cuda:
+                    raise TypeError("Adam8bit needs fp32 or bf16 CUDA parameters")
                 if p.grad.is_sparse:
                     raise TypeError("sparse gradients are not supported")
                 st = self._state_for(p)
                 if st["m_absmax"].numel() != num_blocks(p.numel()):
                     raise ValueError("state does not match the parameter size")
                 st["step"] += 1
-                buckets[(p.device, p.grad.dtype, st["step"])].append(p)
+                buckets[(p.device, p.dtype, p.grad.dtype, st["step"])].append(p)
             b1, b2 = group["betas"]
-            for (dev, gdt, t), ps in buckets.items():
+            for (dev, pdt, gdt, t), ps in buckets.items():
                 grads = [q.grad if q.grad.is_contiguous() else q.grad.contiguous() for q in ps]
                 sts = [self.state[q] for q in ps]
-                key = (gi, dev, gdt)
+                key = (gi, dev, pdt, gdt)
                 ptrs = tuple(x.data_ptr() for x in ps) + tuple(x.data_ptr() for x in grads)
                 cached = self._args_cache.get(key)
                 if cached is None or cached[0] != ptrs:

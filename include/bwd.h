@@ -150,6 +150,21 @@ bwd_status bwd_adam8bit_step_multi(int32_t num_tensors, float* const* p,
                                    float* const* v_absmax, const int64_t* n,
                                    const bwd_adam_hparams* hp, void* stream);
 
+/* The multi-tensor step with the parameter type given: p_dtype BWD_F32
+ * (as bwd_adam8bit_step_multi) or BWD_BF16.  bf16 parameters are widened to
+ * fp32 for the update and stored back rounded to nearest even (the page's
+ * low-precision state with a high-precision update, section 二, opening
+ * paragraph); codes and absmax are the same as with fp32 parameters.
+ *   p : HOST array of num_tensors device pointers to fp32[n] or bf16[n]
+ *       parameters, updated in place.  Other arguments as above. */
+bwd_status bwd_adam8bit_step_multi_ex(int32_t num_tensors, void* const* p,
+                                      bwd_dtype p_dtype, const void* const* g,
+                                      bwd_dtype g_dtype, uint8_t* const* m_codes,
+                                      float* const* m_absmax,
+                                      uint8_t* const* v_codes,
+                                      float* const* v_absmax, const int64_t* n,
+                                      const bwd_adam_hparams* hp, void* stream);
+
 /* Static description of a status code. */
 const char* bwd_status_string(bwd_status status);
 

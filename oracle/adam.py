@@ -26,6 +26,10 @@ Readings where the page is silent:
   t counts from 1; the state before step 1 is all codes of +0.0 with absmax 0
   (R6), which dequantizes to exact zeros.  bf16 gradients widen exactly.
 
+bf16 parameters (the page's low-precision weights with a high-precision
+update): p is widened to binary32, updated as above, and rounded back to bf16
+(nearest, ties to even).
+
 Decoupled weight decay (AdamW; not on the page, the first extension of the
 method): with weight_decay wd > 0 the parameters are first scaled,
 p = p * f32(1 - lr * wd) (factor formed in binary64), then updated as above
@@ -88,6 +92,20 @@ def widen_bf16(bits) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32)
 
 
+def round_to_bf16(x) -> np.ndarray:
+    """binary32 -> bf16 bit patterns, round to nearest, ties to even: keep
+    the high 16 bits, add one unit when the dropped 16 bits exceed half a
+    unit, or equal it and the kept part is odd.  NaNs stay NaN (quiet)."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    hi = u >> 16
+    lo = u & 0xFFFF
+    up = (lo > 0x8000) | ((lo == 0x8000) & ((hi & 1) == 1))
+    r = (hi + up.astype(np.uint64)).astype(np.uint32)
+    nan = np.isnan(np.asarray(x, dtype=np.float32))
+    r[nan] = (hi[nan] | 0x40).astype(np.uint32)
+    return r.astype(np.uint16)
+
+
 def adam_update_fp32(p, g, m_old, v_old, hp: AdamHParams):
     """One binary32 Adam(W) update (R10).  Returns new (p, m, v); inputs unchanged."""
     if hp.weight_decay < 0.0:
@@ -105,14 +123,20 @@ def adam_update_fp32(p, g, m_old, v_old, hp: AdamHParams):
     return p_new.astype(F32), m.astype(F32), v.astype(F32)
 
 
-def adam8bit_step(p, g, m_codes, m_absmax, v_codes, v_absmax, hp: AdamHParams):
+def adam8bit_step(p, g, m_codes, m_absmax, v_codes, v_absmax, hp: AdamHParams, p_bf16: bool = False):
     """One 8-bit Adam step on one flat tensor (R9-R11).
 
-    Returns new ``(p, m_codes, m_absmax, v_codes, v_absmax)``.
+    Returns new ``(p, m_codes, m_absmax, v_codes, v_absmax)``.  With
+    ``p_bf16`` the parameters are bf16 bit patterns (uint16): they are
+    widened to binary32 for the update and rounded back to bf16.
     """
     m_old = dequantize_blockwise(m_codes, m_absmax, signed=True)
     v_old = dequantize_blockwise(v_codes, v_absmax, signed=False)
-    p_new, m, v = adam_update_fp32(p, g, m_old, v_old, hp)
+    if p_bf16:
+        p32, m, v = adam_update_fp32(widen_bf16(p), g, m_old, v_old, hp)
+        p_new = round_to_bf16(p32)
+    else:
+        p_new, m, v = adam_update_fp32(p, g, m_old, v_old, hp)
     mc, ma = quantize_blockwise(m, signed=True)
     vc, va = quantize_blockwise(v, signed=False)
     return p_new, mc, ma, vc, va

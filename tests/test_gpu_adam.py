@@ -338,3 +338,62 @@ def test_step_on_tensor_larger_than_2p31_elements(bwd):
         compare_step(got, ref)
     del p, g, mc, ma, vc, va
     torch.cuda.empty_cache()
+
+
+def compare_bf16_params(p_bits, ref_bits):
+    """bf16 parameters: at most 1e-3 of them one bf16 unit apart (the fp32
+    update is within a few ulps, so it can land on the other side of a bf16
+    rounding boundary), none further."""
+    a = p_bits.astype(np.int32)
+    b = ref_bits.astype(np.int32)
+    d = np.abs(a - b)
+    assert d.max(initial=0) <= 1
+    assert np.count_nonzero(d) <= max(1e-3 * d.size, 2)
+
+
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
+def test_bf16_params_step_from_identical_state(bwd, gdt):
+    from oracle.adam import round_to_bf16
+
+    rng = np.random.default_rng(31)
+    sizes = [3 * B + 7, 2048, 5000]
+    ps = [torch.from_numpy(round_to_bf16((rng.standard_normal(n) * 0.02).astype(np.float32)).view(np.int16))
+          .view(torch.bfloat16) for n in sizes]
+    gs = [W.gen_normal(n, 1e-2, 40 + i, dtype=gdt) for i, n in enumerate(sizes)]
+    sts = [random_state(n, 50 + i) for i, n in enumerate(sizes)]
+    dp = [p.to(DEV) for p in ps]
+    dst = [to_dev(*st) for st in sts]
+    hp = oracle.AdamHParams(lr=1e-3, weight_decay=0.01, step=4)
+    bwd.adam8bit_step_multi(dp, [g.to(DEV) for g in gs], *[[s[k] for s in dst] for k in range(4)],
+                            lr=hp.lr, weight_decay=hp.weight_decay, step=hp.step)
+    torch.cuda.synchronize()
+    for i in range(len(sizes)):
+        pb = ps[i].view(torch.int16).numpy().view(np.uint16)
+        ref = oracle.adam8bit_step(pb, g_to_np(gs[i]), *sts[i], hp, p_bf16=True)
+        got_p = dp[i].cpu().view(torch.int16).numpy().view(np.uint16)
+        compare_bf16_params(got_p, ref[0])
+        for a, b in zip((x.cpu().numpy() for x in dst[i]), ref[1:]):
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def test_bf16_param_optimizer_and_single_tensor_call(bwd):
+    from oracle.adam import widen_bf16
+
+    torch.manual_seed(5)
+    p = torch.nn.Parameter((torch.randn(6000, device=DEV) * 0.02).to(torch.bfloat16))
+    opt = bwd.Adam8bit([p], lr=1e-3)
+    ref = (p.detach().cpu().view(torch.int16).numpy().view(np.uint16).copy(), *oracle.state_init(6000))
+    for t in range(1, 4):
+        g = torch.randn(6000, device=DEV, dtype=torch.bfloat16) * 1e-2
+        p.grad = g
+        opt.step()
+        ref = oracle.adam8bit_step(ref[0], widen_bf16(g.cpu().view(torch.int16).numpy().view(np.uint16)), *ref[1:],
+                                   oracle.AdamHParams(lr=1e-3, step=t), p_bf16=True)
+    st = opt.state[p]
+    compare_bf16_params(p.detach().cpu().view(torch.int16).numpy().view(np.uint16), ref[0])
+    assert np.array_equal(st["m_codes"].cpu().numpy(), ref[1]) and np.array_equal(st["v_codes"].cpu().numpy(), ref[3])
+    # the single-tensor call routes bf16 parameters through the typed entry point
+    q = p.detach().clone().view(-1)
+    mc, ma, vc, va = bwd.state_init(q.numel(), DEV)
+    bwd.adam8bit_step(q, p.grad.view(-1), mc, ma, vc, va, lr=1e-3, step=1)
+    assert q.dtype == torch.bfloat16

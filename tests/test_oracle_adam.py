@@ -193,3 +193,35 @@ def test_decay_only_step_closed_form():
     np.testing.assert_allclose(p1, p * (1 - 2e-3 * 0.05), rtol=1e-6)
     with pytest.raises(ValueError):
         oracle.adam_update_fp32(p, z, z, z, oracle.AdamHParams(weight_decay=-1.0))
+
+
+def test_bf16_rounding_matches_torch():
+    """round_to_bf16 against torch's float32 -> bfloat16 conversion (round to
+    nearest even), on random values, ties and boundary patterns."""
+    from oracle.adam import round_to_bf16
+
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal(200_000) * 10.0 ** rng.uniform(-30, 30, 200_000)).astype(np.float32)
+    base = rng.integers(0, 1 << 16, 2000, dtype=np.uint32) << 16
+    ties = np.concatenate([base | 0x8000, base | 0x7FFF, base | 0x8001, base]).view(np.float32)
+    ties = ties[np.isfinite(ties)]
+    for arr in (x, ties, np.array([0.0, -0.0, 1.0, -1.0, 3.3895314e38, 1e-40], np.float32)):
+        want = torch.from_numpy(arr).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(round_to_bf16(arr), want)
+
+
+def test_8bit_step_with_bf16_params_rounds_the_fp32_update():
+    from oracle.adam import round_to_bf16, widen_bf16
+
+    rng = np.random.default_rng(13)
+    n = 2 * B + 9
+    p = round_to_bf16((rng.standard_normal(n) * 0.02).astype(np.float32))
+    g = (rng.standard_normal(n) * 1e-2).astype(np.float32)
+    st = oracle.state_init(n)
+    hp = oracle.AdamHParams(lr=1e-3, step=1)
+    out = oracle.adam8bit_step(p, g, *st, hp, p_bf16=True)
+    ref32 = oracle.adam8bit_step(widen_bf16(p), g, *st, hp)
+    assert out[0].dtype == np.uint16
+    assert np.array_equal(out[0], round_to_bf16(ref32[0]))
+    for a, b in zip(out[1:], ref32[1:]):
+        assert np.array_equal(a, b)
