@@ -54,7 +54,7 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--param-dtype", default="f32", choices=["f32", "bf16"],
                     help="parameter storage (bf16: widened for the update, rounded back)")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 

@@ -120,6 +120,12 @@ __device__ __forceinline__ uint32_t ld_stream_u1(const void* p) {
 
 
 
+// Hint: bring `bytes` (multiple of 16, 16-byte aligned) of global memory into
+// L2.  Nothing waits for it, so it cannot stall or hang anything.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Code of a normalised value (see the count tables in tables.h).  The clamps
 // keep any bit pattern, non-finite ones included, inside the tables.
 __device__ __forceinline__ uint32_t code_signed(float q, const bwd::Tables& tab) {
@@ -229,6 +235,10 @@ quantize_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ co
     const int64_t base = b * BWD_BLOCK;
     const int rem = static_cast<int>(rem_in_block(n, base));
     const bool vec = vec_ok && rem == BWD_BLOCK;
+    if (t == 0 && vec_ok) {  // ask L2 for the group's next block
+      const int64_t bn = b + stride;
+      if (bn < nb && n - bn * BWD_BLOCK >= BWD_BLOCK) prefetch_l2(x + bn * BWD_BLOCK, 8192u);
+    }
     float v[kPer];
     if (vec) {
 #pragma unroll
@@ -317,6 +327,8 @@ __global__ void fill_kernel(uint8_t* __restrict__ a, uint8_t va, uint8_t* __rest
     fb[i] = 0.0f;
   }
 }
+
+
 
 // --------------------------------------------------------------------------
 // 8-bit Adam
@@ -407,6 +419,7 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
     if (args.block_start[mid] <= gb) lo = mid; else hi = mid - 1;
   }
   int ti = lo;
+  int tn = lo;  // tensor of the block prefetched one iteration ahead (threads 0-3)
 
   const float b1 = args.b1, omb1 = args.omb1, b2 = args.b2, omb2 = args.omb2;
   const float eps = args.eps, step_size = args.step_size, inv_bc2s = args.inv_bc2s, decay = args.decay;
@@ -423,6 +436,22 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
     const bool vec = T.vec && rem == BWD_BLOCK;
     const float ma_old = T.ma[lb];
     const float va_old = T.va[lb];
+    // four threads ask L2 for the group's next block, one array each, so
+    // that block's loads find it there instead of in DRAM
+    if (t < 4) {
+      const int64_t gn = gb + stride;
+      if (gn < total) {
+        while (args.block_start[tn + 1] <= gn) ++tn;
+        const TensorArgs& N = args.t[tn];
+        const int64_t bn = (gn - args.block_start[tn]) * BWD_BLOCK;
+        if (N.vec && N.n - bn >= BWD_BLOCK) {
+          if (t == 0) prefetch_l2(static_cast<const char*>(N.p) + bn * (kPBf16 ? 2 : 4), kPBf16 ? 4096u : 8192u);
+          else if (t == 1) prefetch_l2(static_cast<const char*>(N.g) + bn * (kBf16 ? 2 : 4), kBf16 ? 4096u : 8192u);
+          else if (t == 2) prefetch_l2(N.mc + bn, 2048u);
+          else prefetch_l2(N.vc + bn, 2048u);
+        }
+      }
+    }
 
     float p[kPer], g[kPer];
     uint32_t mw[kQuads], vw[kQuads];
