@@ -1,4 +1,4 @@
-// Host builder of the dynamic-tree maps, thresholds and the count table.
+// Host builder of the dynamic-tree maps, thresholds and the bucket entries.
 //
 // "8-BIT OPTIMIZERS VIA BLOCK-WISE QUANTIZATION", section 二 / 动态量化: an
 // 8-bit dynamic tree number is a sign bit, an exponent counted as leading
@@ -77,34 +77,60 @@ float from_bits(uint32_t u) {
   return f;
 }
 
-// One bucket: values from v_lo to v_hi (v_lo <= v_hi).  Stores the count of
-// thresholds <= v_lo and checks that (v_lo, v_hi] holds at most one more.
-int fill_bucket(const float* t, float v_lo, float v_hi, uint8_t* out, char* err, size_t errlen) {
+int count_le(const float* t, float v) {
   int c = 0;
-  while (c < kCodes - 1 && t[c] <= v_lo) ++c;
-  *out = static_cast<uint8_t>(c);
-  if (c + 1 < kCodes - 1 && !(t[c + 1] > v_hi)) {
-    std::snprintf(err, errlen, "bucket [%a, %a] holds two thresholds", v_lo, v_hi);
-    return -1;
+  while (c < kCodes - 1 && t[c] <= v) ++c;
+  return c;
+}
+
+uint32_t to_bits(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  return u;
+}
+
+// Entry of one bucket of one sign whose values run from v_lo to v_hi
+// (v_lo <= v_hi).  `shift` and `low_mask` split a pattern into bucket and
+// low bits; negative buckets complement the low bits.  Fails if the bucket
+// holds two thresholds, or a threshold outside its pattern range (possible
+// only in a clamped first bucket).
+int make_entry(const float* t, float v_lo, float v_hi, uint32_t shift, uint32_t low_mask, bool negative,
+               uint32_t* out, char* err, size_t errlen) {
+  const int c = count_le(t, v_lo);
+  uint32_t tl = 1u << kSgnShift;  // no threshold: above every low value of either map
+  if (c < kCodes - 1 && t[c] <= v_hi) {
+    if (c + 1 < kCodes - 1 && t[c + 1] <= v_hi) {
+      std::snprintf(err, errlen, "bucket [%a, %a] holds two thresholds", v_lo, v_hi);
+      return -1;
+    }
+    const uint32_t tb = to_bits(t[c]);
+    if ((tb >> shift) != (to_bits(negative ? v_lo : v_hi) >> shift)) {
+      std::snprintf(err, errlen, "threshold %a lies outside the patterns of bucket [%a, %a]", t[c], v_lo, v_hi);
+      return -1;
+    }
+    tl = negative ? ((tb & low_mask) ^ low_mask) : (tb & low_mask);
   }
+  *out = (static_cast<uint32_t>(c) << kEntShift) + (1u << kEntShift) - tl;
   return 0;
 }
 
-int build_counts(const float* ts, const float* tu, uint8_t* cnt, char* err, size_t errlen) {
-  std::memset(cnt, 255, kCntPad);  // buckets no normalised value reaches
-  const uint32_t sh = kCntSignedShift, low = (1u << kCntSignedShift) - 1u;
-  for (uint32_t i = 0; i <= (kCntSignedMax & 0x1fffu); ++i) {
-    // non-negative patterns: the lowest value has the smallest pattern
-    if (fill_bucket(ts, from_bits(i << sh), from_bits((i << sh) | low), &cnt[i], err, errlen) != 0) return -1;
-    // negative patterns: the lowest value has the largest pattern
-    const uint32_t n = i | 0x4000u;
-    if (fill_bucket(ts, from_bits((n << sh) | low), from_bits(n << sh), &cnt[n], err, errlen) != 0) return -1;
+int build_entries(const float* ts, const float* tu, uint32_t* ent, char* err, size_t errlen) {
+  for (int i = 0; i < kEntries; ++i) ent[i] = 255u << kEntShift;  // padding, never read
+  for (uint32_t h = kSgnLo; h <= kSgnHi; ++h) {
+    // the first bucket of each sign also takes every smaller magnitude
+    // (down to +0.0, and down to the smallest negative subnormal: -0.0 is
+    // handed to the lookup as +0.0)
+    const float top = from_bits((h << kSgnShift) | kSgnLowMask);
+    const float pos_lo = h == kSgnLo ? 0.0f : from_bits(h << kSgnShift);
+    const float neg_hi = h == kSgnLo ? -from_bits(1u) : -from_bits(h << kSgnShift);
+    if (make_entry(ts, pos_lo, top, kSgnShift, kSgnLowMask, false, &ent[h - kSgnLo], err, errlen) != 0 ||
+        make_entry(ts, -top, neg_hi, kSgnShift, kSgnLowMask, true, &ent[kSgnN + h - kSgnLo], err, errlen) != 0)
+      return -1;
   }
-  for (uint32_t h = kCntUnsignedLo; h <= kCntUnsignedHi; ++h) {
-    // the first bucket also takes every value below 2^-26
-    const float lo = h == kCntUnsignedLo ? 0.0f : from_bits(h << 16);
-    if (fill_bucket(tu, lo, from_bits((h << 16) | 0xffffu), &cnt[kCntUnsignedOff + h - kCntUnsignedLo], err,
-                    errlen) != 0)
+  for (uint32_t h = kUnsLo; h <= kUnsHi; ++h) {
+    const float lo = h == kUnsLo ? 0.0f : from_bits(h << kUnsShift);
+    if (make_entry(tu, lo, from_bits((h << kUnsShift) | kUnsLowMask), kUnsShift, kUnsLowMask, false,
+                   &ent[kUnsOff + h - kUnsLo], err, errlen) != 0)
       return -1;
   }
   return 0;
@@ -113,11 +139,12 @@ int build_counts(const float* ts, const float* tu, uint8_t* cnt, char* err, size
 }  // namespace
 
 int build_tables(Tables* tab, char* err, size_t errlen) {
+  float thr[2][kCodes];
   for (int k = 0; k < 2; ++k) {
     build_map(k == 0, tab->map[k]);
-    build_thresholds(tab->map[k], tab->thr[k]);
+    build_thresholds(tab->map[k], thr[k]);
   }
-  return build_counts(tab->thr[0], tab->thr[1], tab->cnt, err, errlen);
+  return build_entries(thr[0], thr[1], tab->ent, err, errlen);
 }
 
 }  // namespace bwd

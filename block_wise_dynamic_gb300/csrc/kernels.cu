@@ -18,7 +18,7 @@
 // coalesced.  The block absmax is a warp shuffle
 // reduction and a pass over the group's four warps through shared memory,
 // synchronised by a named barrier per group.  The maps, thresholds and the
-// count table (tables.h) are copied once per CTA into dynamic shared memory.
+// bucket entries (tables.h) are copied once per CTA into dynamic shared memory.
 //
 // Exactness.  Every operation that decides a code is IEEE binary32 with
 // explicit round-to-nearest intrinsics (no contracted multiply-add): the
@@ -126,18 +126,23 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// Code of a normalised value (see the count tables in tables.h).  The clamps
-// keep any bit pattern, non-finite ones included, inside the tables.
+// Code of a normalised value (see the bucket entries in tables.h): one table
+// read.  Signed map: q in [-1, 1] with -0.0 passed as +0.0.  The clamps keep
+// any bit pattern, non-finite ones included, inside the table.
 __device__ __forceinline__ uint32_t code_signed(float q, const bwd::Tables& tab) {
-  const uint32_t c = tab.cnt[min(__float_as_uint(q) >> bwd::kCntSignedShift, bwd::kCntSignedMax)];
-  return c + (tab.thr[0][c] <= q ? 1u : 0u);
+  const uint32_t b = __float_as_uint(q);
+  const uint32_t h = min(__float_as_uint(fmaxf(fabsf(q), __uint_as_float(bwd::kSgnLo << bwd::kSgnShift))) >>
+                             bwd::kSgnShift, bwd::kSgnHi);
+  const uint32_t i = h - bwd::kSgnLo + ((b >> 31) ? bwd::kSgnN : 0u);
+  const uint32_t low = (b ^ static_cast<uint32_t>(static_cast<int32_t>(b) >> 31)) & bwd::kSgnLowMask;
+  return (tab.ent[i] + low) >> bwd::kEntShift;
 }
 
 // Unsigned map, q >= +0 (the second moment is never negative).
 __device__ __forceinline__ uint32_t code_unsigned_nonneg(float q, const bwd::Tables& tab) {
-  const uint32_t h = min(max(__float_as_uint(q) >> 16, bwd::kCntUnsignedLo), bwd::kCntUnsignedHi);
-  const uint32_t c = tab.cnt[h + (bwd::kCntUnsignedOff - bwd::kCntUnsignedLo)];
-  return c + (tab.thr[1][c] <= q ? 1u : 0u);
+  const uint32_t b = __float_as_uint(q);
+  const uint32_t h = min(max(b >> bwd::kUnsShift, bwd::kUnsLo), bwd::kUnsHi);
+  return (tab.ent[bwd::kUnsOff - bwd::kUnsLo + h] + (b & bwd::kUnsLowMask)) >> bwd::kEntShift;
 }
 
 // Unsigned map, any sign: every threshold is positive, so a negative input
@@ -153,8 +158,9 @@ __device__ __forceinline__ uint32_t code_unsigned(float q, const bwd::Tables& ta
 // negative one can change a code (-0.0 -> code 128, a negative subnormal ->
 // code 127).  Read as signed integers, the bit patterns of -0.0 and of the
 // negative values closest to zero are the smallest of all, so one integer
-// min over the quotients flags a block that has one; its values are then
-// redone with IEEE division.
+// min over the quotients flags a block that has one (a -0.0 quotient
+// included); its values with the sign bit set are then redone with IEEE
+// division, and a zero quotient is looked up as +0.0.
 template <bool kSigned, bool kAnySign>
 __device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, const bwd::Tables& tab,
                                                uint32_t (&w)[kQuads]) {
@@ -176,13 +182,14 @@ __device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, 
       if (kSigned && minb <= static_cast<int>(0x8E000000u)) {
 #pragma unroll
         for (int j = 0; j < kPer; ++j)
-          if (x[j] < 0.0f && bwd::div_fast(d, x[j]) > -0x1p-99f) c[j] = code_signed(__fdiv_rn(x[j], a), tab);
+          if (__float_as_int(x[j]) < 0 && bwd::div_fast(d, x[j]) > -0x1p-99f)
+            c[j] = code_signed(__fadd_rn(__fdiv_rn(x[j], a), 0.0f), tab);  // -0.0 -> +0.0
       }
     } else {
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
         const float q = __fdiv_rn(x[j], a);
-        c[j] = kSigned ? code_signed(q, tab) : code_unsigned(q, tab);
+        c[j] = kSigned ? code_signed(__fadd_rn(q, 0.0f), tab) : code_unsigned(q, tab);
       }
     }
   }

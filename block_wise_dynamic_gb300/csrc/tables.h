@@ -3,29 +3,35 @@
 // A quantization code is the index of the nearest entry of a 256-entry
 // ascending map ("8-BIT OPTIMIZERS VIA BLOCK-WISE QUANTIZATION", section 二 /
 // 动态量化).  It equals the number of decision thresholds t[i] (midpoints of
-// neighbouring entries) that are <= the normalised value q.  Besides the maps
-// and the thresholds the kernels use one more table to find that count
-// without a search:
+// neighbouring entries) that are <= the normalised value q.  The kernels find
+// that count with one table read and no search:
 //
-//   count tables.  Binary32 values whose bit patterns agree in their top bits
-//   form a bucket.  For a bucket with lowest value v_lo (the most negative
-//   one for negative patterns), cnt[bucket] = number of thresholds <= v_lo.
-//   The builder checks that no bucket holds more than one further threshold,
-//   so for any q in the bucket
-//       code(q) = cnt[bucket] + (thr[cnt[bucket]] <= q)
-//   exactly, ties and signed zeros included.
+//   buckets.  Binary32 values of one sign whose bit patterns agree in their
+//   top bits form a bucket.  The builder checks that every bucket holds at
+//   most one threshold, so inside a bucket the count is c (the thresholds
+//   below the bucket) or c + 1 (q at or above the bucket's threshold).
+//   Inside a bucket of positive values, q >= t exactly when the low pattern
+//   bits of q are >= those of t; for negative values the order of the low
+//   bits is reversed, so they are complemented first ("low" below).
 //
-//   Signed map (first moment): bucket = pattern >> 17 (64 buckets per binade,
-//   fine enough because neighbouring signed thresholds are at least 1.4%
-//   apart), [0, 0x1FC0] for [0, 1.016) and [0x4000, 0x5FC0] for (-1.016, -0];
-//   lookups clamp the bucket to 0x5FC0.
-//   Unsigned map (second moment): bucket = pattern >> 16 (128 per binade:
-//   its thresholds are 0.7% apart near 1), clamped to [0x3280, 0x3F80], i.e.
-//   values from 2^-26 (below the smallest threshold, 5e-8) to 1.008; stored
-//   from kCntUnsignedOff on.
-//   Entries no normalised value reaches hold 255.  The tables stay small
-//   (27 KB) on purpose: shared memory and the L1 cache share one array per
-//   SM, and the fused kernel keeps its global loads in flight in L1.
+//   entries.  One 32-bit word per bucket, E = c * 2^18 + (2^18 - tl), with tl
+//   the (complemented, for negative buckets) low bits of the bucket's
+//   threshold, or 2^17 when the bucket has none.  For any low < 2^17,
+//       code(q) = (E + low(q)) >> 18
+//   because 2^18 - tl + low lies in [2^17, 2^19) and reaches 2^18 exactly
+//   when low >= tl.
+//
+//   Signed map (first moment): bucket = |pattern| >> 17 (64 per binade: the
+//   signed thresholds are at least 1.4% apart), clamped to [kSgnLo, kSgnHi]:
+//   magnitudes from 2^-21 (below the smallest nonzero threshold, 5e-7) to
+//   1.016.  Entries [0, kSgnN) are the positive buckets, [kSgnN, 2 kSgnN) the
+//   negative ones.  Every magnitude below 2^-21 shares the first bucket of its
+//   sign; that is exact for all of them but -0.0, whose code (that of +0.0,
+//   128) the kernels obtain by adding +0.0 to a zero quotient first.
+//   Unsigned map (second moment): bucket = pattern >> 16 (128 per binade: its
+//   thresholds are 0.7% apart near 1), clamped to [kUnsLo, kUnsHi] (2^-25,
+//   below the smallest threshold 5e-8, to 1.008), from kUnsOff on.
+//   Buckets above 1 exist only as clamp targets: no normalised value is > 1.
 #pragma once
 
 #include <cstddef>
@@ -34,21 +40,23 @@
 namespace bwd {
 
 constexpr int kCodes = 256;
-constexpr uint32_t kCntSignedShift = 17;
-constexpr uint32_t kCntSignedMax = 0x5FC0u;    // bucket of -1.0 (clamp for signed lookups)
-constexpr uint32_t kCntUnsignedLo = 0x3280u;   // pattern >> 16 of 2^-26
-constexpr uint32_t kCntUnsignedHi = 0x3F80u;   // pattern >> 16 of 1.0
-constexpr uint32_t kCntUnsignedOff = 0x5FD0u;  // where the unsigned buckets start
-constexpr int kCntPad = 27872;                 // kCntUnsignedOff + 0xD01, rounded up to 16
-
-static_assert(kCntUnsignedOff > kCntSignedMax, "unsigned buckets follow the signed ones");
-static_assert(kCntPad >= static_cast<int>(kCntUnsignedOff + kCntUnsignedHi - kCntUnsignedLo + 1), "size");
+constexpr uint32_t kEntShift = 18;                 // code = (entry + low) >> kEntShift
+constexpr uint32_t kSgnShift = 17;                 // signed bucket = |pattern| >> 17
+constexpr uint32_t kSgnLowMask = (1u << kSgnShift) - 1u;
+constexpr uint32_t kSgnLo = 0x1A80u;               // bucket of 2^-21
+constexpr uint32_t kSgnHi = 0x1FC0u;               // bucket of 1.0
+constexpr uint32_t kSgnN = kSgnHi - kSgnLo + 1u;   // buckets per sign
+constexpr uint32_t kUnsShift = 16;                 // unsigned bucket = pattern >> 16
+constexpr uint32_t kUnsLowMask = (1u << kUnsShift) - 1u;
+constexpr uint32_t kUnsLo = 0x3300u;               // pattern >> 16 of 2^-25
+constexpr uint32_t kUnsHi = 0x3F80u;               // pattern >> 16 of 1.0
+constexpr uint32_t kUnsOff = 2u * kSgnN;           // where the unsigned entries start
+constexpr int kEntries = static_cast<int>((kUnsOff + kUnsHi - kUnsLo + 1u + 3u) / 4u * 4u);
 
 // Index 0: signed map (first moment), 1: unsigned map (second moment).
 struct Tables {
-  float map[2][kCodes];   // ascending values
-  float thr[2][kCodes];   // 255 thresholds, [255] = +inf
-  uint8_t cnt[kCntPad];   // count tables, both maps
+  float map[2][kCodes];    // ascending values
+  uint32_t ent[kEntries];  // bucket entries, both maps
 };
 
 static_assert(sizeof(Tables) % 16 == 0, "tables are copied as 16-byte words");
