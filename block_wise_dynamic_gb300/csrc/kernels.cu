@@ -126,29 +126,30 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// Code of a normalised value (see the bucket entries in tables.h): one table
-// read.  Signed map: q in [-1, 1] with -0.0 passed as +0.0.  The clamps keep
-// any bit pattern, non-finite ones included, inside the table.
-__device__ __forceinline__ uint32_t code_signed(float q, const bwd::Tables& tab) {
+// Code word of a normalised value (see the bucket entries in tables.h): one
+// table read; the code is the word's top byte.  Signed map: q in [-1, 1]
+// with -0.0 passed as +0.0.  The clamps keep any bit pattern, non-finite ones
+// included, inside the table.
+__device__ __forceinline__ uint32_t code_word_signed(float q, const bwd::Tables& tab) {
   const uint32_t b = __float_as_uint(q);
   const uint32_t h = min(__float_as_uint(fmaxf(fabsf(q), __uint_as_float(bwd::kSgnLo << bwd::kSgnShift))) >>
                              bwd::kSgnShift, bwd::kSgnHi);
   const uint32_t i = h - bwd::kSgnLo + ((b >> 31) ? bwd::kSgnN : 0u);
   const uint32_t low = (b ^ static_cast<uint32_t>(static_cast<int32_t>(b) >> 31)) & bwd::kSgnLowMask;
-  return (tab.ent[i] + low) >> bwd::kEntShift;
+  return tab.ent[i] + low;
 }
 
 // Unsigned map, q >= +0 (the second moment is never negative).
-__device__ __forceinline__ uint32_t code_unsigned_nonneg(float q, const bwd::Tables& tab) {
+__device__ __forceinline__ uint32_t code_word_unsigned_nonneg(float q, const bwd::Tables& tab) {
   const uint32_t b = __float_as_uint(q);
   const uint32_t h = min(max(b >> bwd::kUnsShift, bwd::kUnsLo), bwd::kUnsHi);
-  return (tab.ent[bwd::kUnsOff - bwd::kUnsLo + h] + (b & bwd::kUnsLowMask)) >> bwd::kEntShift;
+  return tab.ent[bwd::kUnsOff - bwd::kUnsLo + h] + (b & bwd::kUnsLowMask);
 }
 
 // Unsigned map, any sign: every threshold is positive, so a negative input
-// has code 0.
-__device__ __forceinline__ uint32_t code_unsigned(float q, const bwd::Tables& tab) {
-  const uint32_t c = code_unsigned_nonneg(q, tab);
+// has code 0 (word 0).
+__device__ __forceinline__ uint32_t code_word_unsigned(float q, const bwd::Tables& tab) {
+  const uint32_t c = code_word_unsigned_nonneg(q, tab);
   return (__float_as_uint(q) >> 31) ? 0u : c;
 }
 
@@ -164,10 +165,10 @@ __device__ __forceinline__ uint32_t code_unsigned(float q, const bwd::Tables& ta
 template <bool kSigned, bool kAnySign>
 __device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, const bwd::Tables& tab,
                                                uint32_t (&w)[kQuads]) {
-  uint32_t c[kPer];
+  uint32_t c[kPer];  // code words (code in the top byte)
   if (a == 0.0f) {
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) c[j] = kSigned ? 128u : 0u;
+    for (int j = 0; j < kPer; ++j) c[j] = kSigned ? (128u << 24) : 0u;
   } else {
     const bwd::Divisor d = bwd::make_divisor(a, 1u);
     if (d.fast) {
@@ -176,25 +177,26 @@ __device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, 
       for (int j = 0; j < kPer; j += 2) {
         const float2 q = bwd::div_fast2(d, make_float2(x[j], x[j + 1]));
         if (kSigned) minb = min(minb, min(__float_as_int(q.x), __float_as_int(q.y)));
-        c[j] = kSigned ? code_signed(q.x, tab) : (kAnySign ? code_unsigned(q.x, tab) : code_unsigned_nonneg(q.x, tab));
-        c[j + 1] = kSigned ? code_signed(q.y, tab) : (kAnySign ? code_unsigned(q.y, tab) : code_unsigned_nonneg(q.y, tab));
+        c[j] = kSigned ? code_word_signed(q.x, tab) : (kAnySign ? code_word_unsigned(q.x, tab) : code_word_unsigned_nonneg(q.x, tab));
+        c[j + 1] = kSigned ? code_word_signed(q.y, tab) : (kAnySign ? code_word_unsigned(q.y, tab) : code_word_unsigned_nonneg(q.y, tab));
       }
       if (kSigned && minb <= static_cast<int>(0x8E000000u)) {
 #pragma unroll
         for (int j = 0; j < kPer; ++j)
           if (__float_as_int(x[j]) < 0 && bwd::div_fast(d, x[j]) > -0x1p-99f)
-            c[j] = code_signed(__fadd_rn(__fdiv_rn(x[j], a), 0.0f), tab);  // -0.0 -> +0.0
+            c[j] = code_word_signed(__fadd_rn(__fdiv_rn(x[j], a), 0.0f), tab);  // -0.0 -> +0.0
       }
     } else {
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
         const float q = __fdiv_rn(x[j], a);
-        c[j] = kSigned ? code_signed(__fadd_rn(q, 0.0f), tab) : code_unsigned(q, tab);
+        c[j] = kSigned ? code_word_signed(__fadd_rn(q, 0.0f), tab) : code_word_unsigned(q, tab);
       }
     }
   }
 #pragma unroll
-  for (int k = 0; k < kQuads; ++k) w[k] = pack4(c[4 * k], c[4 * k + 1], c[4 * k + 2], c[4 * k + 3]);
+  for (int k = 0; k < kQuads; ++k)
+    w[k] = __byte_perm(__byte_perm(c[4 * k], c[4 * k + 1], 0x0073), __byte_perm(c[4 * k + 2], c[4 * k + 3], 0x0073), 0x5410);
 }
 
 // Max over the 128 threads of a group; every thread gets the result.

@@ -14,12 +14,15 @@
 //   bits of q are >= those of t; for negative values the order of the low
 //   bits is reversed, so they are complemented first ("low" below).
 //
-//   entries.  One 32-bit word per bucket, E = c * 2^18 + (2^18 - tl), with tl
+//   entries.  One 32-bit word per bucket, E = c * 2^24 + (2^24 - tl), with tl
 //   the (complemented, for negative buckets) low bits of the bucket's
 //   threshold, or 2^17 when the bucket has none.  For any low < 2^17,
-//       code(q) = (E + low(q)) >> 18
-//   because 2^18 - tl + low lies in [2^17, 2^19) and reaches 2^18 exactly
-//   when low >= tl.
+//       code(q) = (E + low(q)) >> 24,  the top byte of the sum,
+//   because 2^24 - tl + low lies in [2^24 - 2^17, 2^24 + 2^17) and reaches
+//   2^24 exactly when low >= tl.  The sum stays below 2^32: a bucket with
+//   c = 255 has no threshold left (E = 2^32 - 2^17), and for c <= 254
+//   E <= 255 * 2^24.  The kernels keep the sums and pack the top bytes of
+//   four of them into one word of codes with byte permutes.
 //
 //   Signed map (first moment): bucket = |pattern| >> 17 (64 per binade: the
 //   signed thresholds are at least 1.4% apart), clamped to [kSgnLo, kSgnHi]:
@@ -40,7 +43,7 @@
 namespace bwd {
 
 constexpr int kCodes = 256;
-constexpr uint32_t kEntShift = 18;                 // code = (entry + low) >> kEntShift
+constexpr uint32_t kEntShift = 24;                 // code = (entry + low) >> kEntShift
 constexpr uint32_t kSgnShift = 17;                 // signed bucket = |pattern| >> 17
 constexpr uint32_t kSgnLowMask = (1u << kSgnShift) - 1u;
 constexpr uint32_t kSgnLo = 0x1A80u;               // bucket of 2^-21

@@ -6,7 +6,8 @@
 // The thresholds come from the file named by argv[1] (255 signed, then 255
 // unsigned binary32 values, written by the test from the CPU oracle); the
 // entries come from the library's own builder.  The two lookups below
-// restate code_signed / code_unsigned_nonneg of csrc/kernels.cu on the host:
+// restate code_word_signed / code_word_unsigned_nonneg of csrc/kernels.cu (whose
+// top byte is the code) on the host:
 // the kernels hand -0.0 to the signed lookup as +0.0, and so does this check.
 #include <atomic>
 #include <cmath>
