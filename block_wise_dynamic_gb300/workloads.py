@@ -21,6 +21,13 @@ is synthetic):
   ragged_2000    2,000 fp32 tensors, sizes floor(exp(U(ln 1e3, ln 2^24)))
                  (NumPy default_rng(0)), per-tensor sigma exp(U(ln 1e-5,
                  ln 1e-1)); g fp32 ~ N(0, sigma)
+
+Stable embedding layer (lookup + LayerNorm):
+  embed_7b       Llama-2-7B's token embedding, V 32,000 x D 4,096, a batch of
+                 4 sequences x 4,096 tokens = 16,384 token ids drawn with
+                 Zipf frequencies p(rank k) ~ 1 / (k + 1) (natural
+                 text's rank-frequency shape), ranks mapped to ids by a
+                 seeded permutation; dL/dy ~ N(0, 1)
 """
 
 from __future__ import annotations
@@ -126,3 +133,23 @@ def quant_input(n: int = 1 << 28, seed: int = 0, device="cpu") -> torch.Tensor:
     idx = torch.from_numpy(rng.choice(n, size=k, replace=False).astype(np.int64)).to(device)
     x[idx] *= 100.0
     return x
+
+
+EMBED_7B = (32000, 4096, 4 * 4096)  # V, D, tokens per step
+
+
+def token_ids(count: int, vocab: int, seed: int, zipf_s: float = 1.0, device="cpu") -> torch.Tensor:
+    """int64 token ids with Zipf-like frequencies: rank k has probability
+    proportional to 1 / (k + 1)^zipf_s, ranks permuted over the vocabulary."""
+    rng = np.random.default_rng(seed)
+    p = 1.0 / np.arange(1, vocab + 1, dtype=np.float64) ** zipf_s
+    p /= p.sum()
+    ranks = rng.choice(vocab, size=count, p=p)
+    ids = rng.permutation(vocab)[ranks]
+    return torch.from_numpy(ids.astype(np.int64)).to(device)
+
+
+def random_words(count: int, seed: int, device="cpu") -> torch.Tensor:
+    """Uniform 32-bit random words (as int32 storage), e.g. for initialisers."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(-(2 ** 31), 2 ** 31, (count,), dtype=torch.int64, generator=g).to(torch.int32).to(device)

@@ -26,6 +26,9 @@ Modules
   codebook  -- the signed / unsigned dynamic-tree maps and their thresholds
   blockwise -- block-wise quantize / dequantize
   adam      -- the fp32 Adam update and the 8-bit Adam step (single, list)
+  stable_embedding -- the stable embedding layer (section 二 / 稳定的词嵌入层):
+               Xavier-uniform initialisation, lookup + LayerNorm forward and
+               backward (binary64); imported as ``oracle.stable_embedding``
 
 Parity status per function is listed in each module's header.
 """
