@@ -64,6 +64,12 @@ _SIGNATURES = {
         _int,
         [_i32, _pp, _int, _pp, _int, _pp, _pp, _pp, _pp, ctypes.POINTER(_i64), ctypes.POINTER(AdamHParams), _vp],
     ),
+    "bwd_embedding_init": (_int, [_vp, _i64, _i64, _vp, _vp]),
+    "bwd_embedding_xavier_bound": (ctypes.c_float, [_i64, _i64]),
+    "bwd_embedding_forward": (
+        _int, [_vp, _i64, _vp, _i64, _i64, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]),
+    "bwd_embedding_backward": (
+        _int, [_vp, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "bwd_status_string": (ctypes.c_char_p, [_int]),
     "bwd_last_error": (ctypes.c_char_p, []),
 }

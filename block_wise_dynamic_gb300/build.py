@@ -1,8 +1,9 @@
 """Builds the C-ABI shared library ``libbwd.so`` in-tree for sm_103a.
 
-Two translation units (the host codebook builder and the CUDA kernels) are
-compiled in parallel and linked with the static CUDA runtime, so the library
-depends only on the driver.  No fast-math: every code decision must be IEEE.
+Three translation units (the host codebook builder, the optimizer kernels and
+the stable-embedding kernels) are compiled in parallel and linked with the
+static CUDA runtime, so the library depends only on the driver.  No
+fast-math: every code decision must be IEEE.
 """
 
 from __future__ import annotations
@@ -26,8 +27,9 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-
 SOURCES = {
     "codebook.o": os.path.join(CSRC, "codebook.cpp"),
     "kernels.o": os.path.join(CSRC, "kernels.cu"),
+    "embedding.o": os.path.join(CSRC, "embedding.cu"),
 }
-HEADERS = [os.path.join(CSRC, "tables.h"), os.path.join(INCLUDE, "bwd.h")]
+HEADERS = [os.path.join(CSRC, h) for h in ("tables.h", "exact_div.cuh", "host_util.h")] + [os.path.join(INCLUDE, "bwd.h")]
 
 
 def _nvcc() -> str:

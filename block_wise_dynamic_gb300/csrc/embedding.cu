@@ -1,0 +1,514 @@
+// sm_103a kernels and C ABI of the stable embedding layer.
+//
+// Method: "8-BIT OPTIMIZERS VIA BLOCK-WISE QUANTIZATION" (summary on
+// wiki.neutronadmin.com/news/16836), section 二 / 稳定的词嵌入层: the
+// embedding weight starts from a Xavier-uniform draw, and a layer
+// normalisation follows the lookup so that the layer's output has variance
+// close to 1.  Readings: the Xavier bound is b = sqrt(6 / (V + D)) for a
+// (V, D) weight; the normalisation is LayerNorm over D with biased variance
+// and a learnable scale gamma and shift beta; the backward pass is the
+// gradient of that map, accumulated into the weight rows of the tokens.
+//
+// Work decomposition.  A group of 128 threads owns one token (one row of D
+// fp32 values) at a time and walks the tokens with a grid stride.  On the
+// fast path (D a multiple of 4 and at most 4096, every row pointer 16-byte
+// aligned) thread t of a group holds the float4 chunks t, t + 128, ... of
+// the row in registers, so a row is read from HBM once: every warp access is
+// one contiguous 512-byte span.  Row statistics are sums over the group
+// (warp shuffles, then the group's four warp partials through shared memory
+// in a fixed order, so results do not depend on scheduling).  Forward: mean,
+// then the centred sum of squares from the registers (two passes over the
+// registers, one over memory), then y = (x - mean) rstd gamma + beta.
+// Backward: xhat from the saved mean and rstd, the two sums of
+// g = dy gamma and g xhat, dx = rstd (g - mean(g) - xhat mean(g xhat))
+// added into the weight row with vector reductions (red.global.add.v4.f32;
+// tokens repeat, so the adds are atomic), while each thread accumulates
+// dgamma and dbeta for its own columns in shared memory; each CTA adds its
+// partials into dgamma and dbeta once at the end.  Other shapes take a
+// per-element path with the same arithmetic.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "bwd.h"
+#include "host_util.h"
+
+namespace {
+
+using bwd::host::aligned16;
+using bwd::host::aligned_to;
+using bwd::host::check_launch;
+using bwd::host::cuda_fail;
+using bwd::host::fail;
+
+constexpr int kGroup = 128;                       // threads per token
+constexpr int kGroupWarps = kGroup / 32;          // 4
+constexpr int kChunks = 8;                        // float4 chunks per thread on the fast path
+constexpr int kFastMaxDim = kGroup * 4 * kChunks; // 4096
+constexpr int kFwdGroups = 2;                     // forward CTA: 256 threads
+constexpr int kBwdGroups = 2;                     // backward CTA: 256 threads
+constexpr int kSlowGroups = 2;                    // per-element path: 256 threads
+constexpr int kInitThreads = 256;
+constexpr int kMaxDevices = 64;
+
+// --------------------------------------------------------------------------
+// device helpers
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Named barrier of one 128-thread group (barrier 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "n"(kGroup) : "memory");
+}
+
+// Sums of kVals values over the 128 threads of a group; every thread gets
+// the results.  `red` is the group's [2 slots][kVals][4 warps] scratch; the
+// slot alternates between consecutive calls, so a thread that runs ahead
+// never overwrites partials another thread has yet to read.
+template <int kVals>
+__device__ __forceinline__ void group_sum(float (&v)[kVals], float* red, int slot, int group, int t) {
+  const int lane = t & 31, warp = t >> 5;
+#pragma unroll
+  for (int i = 0; i < kVals; ++i) v[i] = warp_sum(v[i]);
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < kVals; ++i) red[(slot * kVals + i) * kGroupWarps + warp] = v[i];
+  }
+  group_sync(group);
+#pragma unroll
+  for (int i = 0; i < kVals; ++i) {
+    const float4 r = *reinterpret_cast<const float4*>(&red[(slot * kVals + i) * kGroupWarps]);
+    v[i] = __fadd_rn(__fadd_rn(r.x, r.y), __fadd_rn(r.z, r.w));
+  }
+}
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+__device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+
+__device__ __forceinline__ void red_add4(float* p, float4 v) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+
+// --------------------------------------------------------------------------
+// Xavier-uniform initialisation: w = (2 u - 1) b, u = (r >> 8) 2^-24.  The
+// integer converts exactly, 2 u - 1 is exact (a multiple of 2^-23 in
+// [-1, 1)), so the product with the binary32 bound is the one rounding.
+
+__global__ void __launch_bounds__(kInitThreads)
+embed_init_kernel(const uint32_t* __restrict__ words, int64_t n, float bound, float* __restrict__ w) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float u = __fmul_rn(static_cast<float>(words[i] >> 8), 0x1p-24f);
+    w[i] = __fmul_rn(__fsub_rn(__fmul_rn(2.0f, u), 1.0f), bound);
+  }
+}
+
+// --------------------------------------------------------------------------
+// forward: y = LayerNorm(weight[id]); mean and rstd per token (optional).
+// A token id outside [0, V) gives a row of NaN (row 0 is read instead, so
+// no access leaves the weight).
+
+__global__ void __launch_bounds__(kGroup * kFwdGroups, 3)
+embed_fwd_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const float* __restrict__ w, int64_t vocab,
+                 int dim, const float* __restrict__ gamma, const float* __restrict__ beta, float eps,
+                 float* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd) {
+  __shared__ __align__(16) float s_red[kFwdGroups][2 * kGroupWarps];
+  const int group = threadIdx.x / kGroup, t = threadIdx.x % kGroup;
+  const int nch = dim >> 2;
+  const float fdim = static_cast<float>(dim);
+  const float qnan = __int_as_float(0x7fc00000);
+  int slot = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kFwdGroups;
+  for (int64_t tok = static_cast<int64_t>(blockIdx.x) * kFwdGroups + group; tok < num_tokens; tok += stride) {
+    const int64_t id = ids[tok];
+    const bool ok = id >= 0 && id < vocab;
+    const float* row = w + (ok ? id : 0) * static_cast<int64_t>(dim);
+    float4 x[kChunks];
+    float s[1] = {0.0f};
+#pragma unroll
+    for (int k = 0; k < kChunks; ++k) {
+      const int c = t + kGroup * k;
+      if (c < nch) {
+        x[k] = ld4(row + 4 * c);
+        s[0] = __fadd_rn(s[0], __fadd_rn(__fadd_rn(x[k].x, x[k].y), __fadd_rn(x[k].z, x[k].w)));
+      } else {
+        x[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+    }
+    group_sum<1>(s, s_red[group], slot, group, t);
+    slot ^= 1;
+    const float mu = __fdiv_rn(s[0], fdim);
+    float q[1] = {0.0f};
+#pragma unroll
+    for (int k = 0; k < kChunks; ++k) {
+      if (t + kGroup * k < nch) {
+        x[k].x = __fsub_rn(x[k].x, mu);
+        x[k].y = __fsub_rn(x[k].y, mu);
+        x[k].z = __fsub_rn(x[k].z, mu);
+        x[k].w = __fsub_rn(x[k].w, mu);
+        q[0] = __fadd_rn(q[0], __fadd_rn(__fadd_rn(__fmul_rn(x[k].x, x[k].x), __fmul_rn(x[k].y, x[k].y)),
+                                         __fadd_rn(__fmul_rn(x[k].z, x[k].z), __fmul_rn(x[k].w, x[k].w))));
+      }
+    }
+    group_sum<1>(q, s_red[group], slot, group, t);
+    slot ^= 1;
+    const float r = __frsqrt_rn(__fadd_rn(__fdiv_rn(q[0], fdim), eps));
+    float* yrow = y + tok * static_cast<int64_t>(dim);
+#pragma unroll
+    for (int k = 0; k < kChunks; ++k) {
+      const int c = t + kGroup * k;
+      if (c < nch) {
+        const float4 g = ldg4(gamma + 4 * c), b = ldg4(beta + 4 * c);
+        float4 o;
+        o.x = __fadd_rn(__fmul_rn(__fmul_rn(x[k].x, r), g.x), b.x);
+        o.y = __fadd_rn(__fmul_rn(__fmul_rn(x[k].y, r), g.y), b.y);
+        o.z = __fadd_rn(__fmul_rn(__fmul_rn(x[k].z, r), g.z), b.z);
+        o.w = __fadd_rn(__fmul_rn(__fmul_rn(x[k].w, r), g.w), b.w);
+        if (!ok) o = make_float4(qnan, qnan, qnan, qnan);
+        __stcs(reinterpret_cast<float4*>(yrow + 4 * c), o);
+      }
+    }
+    if (t == 0) {
+      if (mean) mean[tok] = ok ? mu : qnan;
+      if (rstd) rstd[tok] = ok ? r : qnan;
+    }
+  }
+}
+
+// Any D and alignment: one element per thread per step, the row re-read
+// from L1/L2 for each pass.
+__global__ void __launch_bounds__(kGroup * kSlowGroups)
+embed_fwd_slow_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const float* __restrict__ w,
+                      int64_t vocab, int64_t dim, const float* __restrict__ gamma, const float* __restrict__ beta,
+                      float eps, float* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd) {
+  __shared__ __align__(16) float s_red[kSlowGroups][2 * kGroupWarps];
+  const int group = threadIdx.x / kGroup, t = threadIdx.x % kGroup;
+  const float fdim = static_cast<float>(dim);
+  const float qnan = __int_as_float(0x7fc00000);
+  int slot = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kSlowGroups;
+  for (int64_t tok = static_cast<int64_t>(blockIdx.x) * kSlowGroups + group; tok < num_tokens; tok += stride) {
+    const int64_t id = ids[tok];
+    const bool ok = id >= 0 && id < vocab;
+    const float* row = w + (ok ? id : 0) * dim;
+    float s[1] = {0.0f};
+    for (int64_t j = t; j < dim; j += kGroup) s[0] = __fadd_rn(s[0], row[j]);
+    group_sum<1>(s, s_red[group], slot, group, t);
+    slot ^= 1;
+    const float mu = __fdiv_rn(s[0], fdim);
+    float q[1] = {0.0f};
+    for (int64_t j = t; j < dim; j += kGroup) {
+      const float d = __fsub_rn(row[j], mu);
+      q[0] = __fadd_rn(q[0], __fmul_rn(d, d));
+    }
+    group_sum<1>(q, s_red[group], slot, group, t);
+    slot ^= 1;
+    const float r = __frsqrt_rn(__fadd_rn(__fdiv_rn(q[0], fdim), eps));
+    float* yrow = y + tok * dim;
+    for (int64_t j = t; j < dim; j += kGroup)
+      yrow[j] = ok ? __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(row[j], mu), r), gamma[j]), beta[j]) : qnan;
+    if (t == 0) {
+      if (mean) mean[tok] = ok ? mu : qnan;
+      if (rstd) rstd[tok] = ok ? r : qnan;
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// backward: dweight[id] += dx, dgamma += dy xhat, dbeta += dy (accumulated).
+// Tokens whose id lies outside [0, V) are skipped.
+
+__host__ __device__ constexpr int bwd_smem_bytes(int dim) { return kBwdGroups * 2 * dim * 4; }
+
+__global__ void __launch_bounds__(kGroup * kBwdGroups, 2)
+embed_bwd_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const float* __restrict__ w, int64_t vocab,
+                 int dim, const float* __restrict__ gamma, const float* __restrict__ mean,
+                 const float* __restrict__ rstd, const float* __restrict__ dy, float* __restrict__ dw,
+                 float* __restrict__ dgamma, float* __restrict__ dbeta) {
+  extern __shared__ __align__(16) float s_part[];  // [group][dgamma | dbeta][dim]
+  __shared__ __align__(16) float s_red[kBwdGroups][2 * 2 * kGroupWarps];
+  const int group = threadIdx.x / kGroup, t = threadIdx.x % kGroup;
+  const int nch = dim >> 2;
+  const float fdim = static_cast<float>(dim);
+  float* const pg = s_part + static_cast<int64_t>(group) * 2 * dim;
+  float* const pb = pg + dim;
+#pragma unroll
+  for (int k = 0; k < kChunks; ++k) {
+    const int c = t + kGroup * k;
+    if (c < nch) {
+      *reinterpret_cast<float4*>(pg + 4 * c) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      *reinterpret_cast<float4*>(pb + 4 * c) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+  }
+  int slot = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kBwdGroups;
+  for (int64_t tok = static_cast<int64_t>(blockIdx.x) * kBwdGroups + group; tok < num_tokens; tok += stride) {
+    const int64_t id = ids[tok];
+    if (id < 0 || id >= vocab) continue;  // the whole group skips together
+    const float mu = mean[tok], r = rstd[tok];
+    const float* row = w + id * static_cast<int64_t>(dim);
+    const float* drow = dy + tok * static_cast<int64_t>(dim);
+    float4 xh[kChunks], d[kChunks];
+    float s[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int k = 0; k < kChunks; ++k) {
+      const int c = t + kGroup * k;
+      if (c < nch) {
+        const float4 x = ld4(row + 4 * c);
+        d[k] = __ldcs(reinterpret_cast<const float4*>(drow + 4 * c));
+        const float4 g = ldg4(gamma + 4 * c);
+        xh[k] = make_float4(__fmul_rn(__fsub_rn(x.x, mu), r), __fmul_rn(__fsub_rn(x.y, mu), r),
+                            __fmul_rn(__fsub_rn(x.z, mu), r), __fmul_rn(__fsub_rn(x.w, mu), r));
+        const float4 gg = make_float4(__fmul_rn(d[k].x, g.x), __fmul_rn(d[k].y, g.y), __fmul_rn(d[k].z, g.z),
+                                      __fmul_rn(d[k].w, g.w));
+        s[0] = __fadd_rn(s[0], __fadd_rn(__fadd_rn(gg.x, gg.y), __fadd_rn(gg.z, gg.w)));
+        s[1] = __fadd_rn(s[1], __fadd_rn(__fadd_rn(__fmul_rn(gg.x, xh[k].x), __fmul_rn(gg.y, xh[k].y)),
+                                         __fadd_rn(__fmul_rn(gg.z, xh[k].z), __fmul_rn(gg.w, xh[k].w))));
+      } else {
+        xh[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        d[k] = xh[k];
+      }
+    }
+    group_sum<2>(s, s_red[group], slot, group, t);
+    slot ^= 1;
+    const float m1 = __fdiv_rn(s[0], fdim), m2 = __fdiv_rn(s[1], fdim);
+    float* dwrow = dw + id * static_cast<int64_t>(dim);
+#pragma unroll
+    for (int k = 0; k < kChunks; ++k) {
+      const int c = t + kGroup * k;
+      if (c < nch) {
+        const float4 g = ldg4(gamma + 4 * c);
+        float4 dx;
+        dx.x = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d[k].x, g.x), m1), __fmul_rn(xh[k].x, m2)));
+        dx.y = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d[k].y, g.y), m1), __fmul_rn(xh[k].y, m2)));
+        dx.z = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d[k].z, g.z), m1), __fmul_rn(xh[k].z, m2)));
+        dx.w = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d[k].w, g.w), m1), __fmul_rn(xh[k].w, m2)));
+        red_add4(dwrow + 4 * c, dx);
+        float4 a = *reinterpret_cast<float4*>(pg + 4 * c);
+        a.x = __fadd_rn(a.x, __fmul_rn(d[k].x, xh[k].x));
+        a.y = __fadd_rn(a.y, __fmul_rn(d[k].y, xh[k].y));
+        a.z = __fadd_rn(a.z, __fmul_rn(d[k].z, xh[k].z));
+        a.w = __fadd_rn(a.w, __fmul_rn(d[k].w, xh[k].w));
+        *reinterpret_cast<float4*>(pg + 4 * c) = a;
+        float4 b = *reinterpret_cast<float4*>(pb + 4 * c);
+        b.x = __fadd_rn(b.x, d[k].x);
+        b.y = __fadd_rn(b.y, d[k].y);
+        b.z = __fadd_rn(b.z, d[k].z);
+        b.w = __fadd_rn(b.w, d[k].w);
+        *reinterpret_cast<float4*>(pb + 4 * c) = b;
+      }
+    }
+  }
+  // the CTA's partials, summed over its groups in a fixed order, go out once
+  __syncthreads();
+  for (int i = threadIdx.x; i < dim; i += blockDim.x) {
+    float a = 0.0f, b = 0.0f;
+#pragma unroll
+    for (int gi = 0; gi < kBwdGroups; ++gi) {
+      a = __fadd_rn(a, s_part[static_cast<int64_t>(gi) * 2 * dim + i]);
+      b = __fadd_rn(b, s_part[static_cast<int64_t>(gi) * 2 * dim + dim + i]);
+    }
+    atomicAdd(dgamma + i, a);
+    atomicAdd(dbeta + i, b);
+  }
+}
+
+__global__ void __launch_bounds__(kGroup * kSlowGroups)
+embed_bwd_slow_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const float* __restrict__ w,
+                      int64_t vocab, int64_t dim, const float* __restrict__ gamma, const float* __restrict__ mean,
+                      const float* __restrict__ rstd, const float* __restrict__ dy, float* __restrict__ dw,
+                      float* __restrict__ dgamma, float* __restrict__ dbeta) {
+  __shared__ __align__(16) float s_red[kSlowGroups][2 * 2 * kGroupWarps];
+  const int group = threadIdx.x / kGroup, t = threadIdx.x % kGroup;
+  const float fdim = static_cast<float>(dim);
+  int slot = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kSlowGroups;
+  for (int64_t tok = static_cast<int64_t>(blockIdx.x) * kSlowGroups + group; tok < num_tokens; tok += stride) {
+    const int64_t id = ids[tok];
+    if (id < 0 || id >= vocab) continue;
+    const float mu = mean[tok], r = rstd[tok];
+    const float* row = w + id * dim;
+    const float* drow = dy + tok * dim;
+    float s[2] = {0.0f, 0.0f};
+    for (int64_t j = t; j < dim; j += kGroup) {
+      const float xh = __fmul_rn(__fsub_rn(row[j], mu), r);
+      const float gg = __fmul_rn(drow[j], gamma[j]);
+      s[0] = __fadd_rn(s[0], gg);
+      s[1] = __fadd_rn(s[1], __fmul_rn(gg, xh));
+    }
+    group_sum<2>(s, s_red[group], slot, group, t);
+    slot ^= 1;
+    const float m1 = __fdiv_rn(s[0], fdim), m2 = __fdiv_rn(s[1], fdim);
+    for (int64_t j = t; j < dim; j += kGroup) {
+      const float xh = __fmul_rn(__fsub_rn(row[j], mu), r);
+      const float d = drow[j];
+      atomicAdd(dw + id * dim + j, __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d, gamma[j]), m1), __fmul_rn(xh, m2))));
+      atomicAdd(dgamma + j, __fmul_rn(d, xh));
+      atomicAdd(dbeta + j, d);
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// host side
+
+struct EmbedDevice {
+  bool ready = false;
+  int num_sms = 0;
+  int occ_fwd = 1;
+  int occ_slow_fwd = 1;
+  int occ_slow_bwd = 1;
+};
+
+std::mutex g_mu;
+EmbedDevice g_dev[kMaxDevices];
+
+bwd_status ensure_device(EmbedDevice** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(BWD_ERR_CUDA, "device ordinal %d unsupported", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  EmbedDevice& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if ((e = cudaFuncSetAttribute(reinterpret_cast<const void*>(embed_bwd_kernel),
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bwd_smem_bytes(kFastMaxDim))) !=
+        cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
+    struct { const void* fn; int threads; int* out; } occ[] = {
+        {reinterpret_cast<const void*>(embed_fwd_kernel), kGroup * kFwdGroups, &d.occ_fwd},
+        {reinterpret_cast<const void*>(embed_fwd_slow_kernel), kGroup * kSlowGroups, &d.occ_slow_fwd},
+        {reinterpret_cast<const void*>(embed_bwd_slow_kernel), kGroup * kSlowGroups, &d.occ_slow_bwd}};
+    for (auto& o : occ) {
+      int v = 0;
+      if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, o.fn, o.threads, 0)) != cudaSuccess)
+        return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+      *o.out = v > 0 ? v : 1;
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return BWD_OK;
+}
+
+// CTAs for `tokens` tokens at `per_cta` tokens at a time: enough to cover
+// them, at most one wave of resident CTAs.
+int grid_for(int64_t tokens, int per_cta, int num_sms, int occ) {
+  const int64_t need = (tokens + per_cta - 1) / per_cta;
+  const int64_t cap = static_cast<int64_t>(num_sms) * occ;
+  return static_cast<int>(need < cap ? need : cap);
+}
+
+bwd_status check_shape(int64_t num_embeddings, int64_t dim) {
+  if (num_embeddings < 1 || dim < 1) return fail(BWD_ERR_INVALID_ARG, "num_embeddings and dim must be >= 1");
+  if (num_embeddings > INT64_MAX / dim) return fail(BWD_ERR_INVALID_ARG, "num_embeddings * dim overflows");
+  return BWD_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// C ABI
+
+extern "C" {
+
+bwd_status bwd_embedding_init(const uint32_t* words, int64_t num_embeddings, int64_t dim, float* weight,
+                              void* stream) {
+  bwd_status s = check_shape(num_embeddings, dim);
+  if (s != BWD_OK) return s;
+  if (!words || !weight) return fail(BWD_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned_to(words, 4) || !aligned_to(weight, 4))
+    return fail(BWD_ERR_INVALID_ARG, "pointer not aligned to its element size");
+  EmbedDevice* d = nullptr;
+  if ((s = ensure_device(&d)) != BWD_OK) return s;
+  const int64_t n = num_embeddings * dim;
+  const float bound = static_cast<float>(std::sqrt(6.0 / (static_cast<double>(num_embeddings) + static_cast<double>(dim))));
+  const int64_t need = (n + kInitThreads - 1) / kInitThreads;
+  const int64_t cap = static_cast<int64_t>(d->num_sms) * 8;
+  embed_init_kernel<<<static_cast<int>(need < cap ? need : cap), kInitThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      words, n, bound, weight);
+  return check_launch("embed_init_kernel launch");
+}
+
+float bwd_embedding_xavier_bound(int64_t num_embeddings, int64_t dim) {
+  if (num_embeddings < 1 || dim < 1) return -1.0f;
+  return static_cast<float>(std::sqrt(6.0 / (static_cast<double>(num_embeddings) + static_cast<double>(dim))));
+}
+
+bwd_status bwd_embedding_forward(const int64_t* ids, int64_t num_tokens, const float* weight, int64_t num_embeddings,
+                                 int64_t dim, const float* gamma, const float* beta, float eps, float* y,
+                                 float* mean, float* rstd, void* stream) {
+  bwd_status s = check_shape(num_embeddings, dim);
+  if (s != BWD_OK) return s;
+  if (num_tokens < 0) return fail(BWD_ERR_INVALID_ARG, "num_tokens < 0");
+  if (!std::isfinite(eps) || eps < 0.0f) return fail(BWD_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (num_tokens > INT64_MAX / dim) return fail(BWD_ERR_INVALID_ARG, "num_tokens * dim overflows");
+  if (num_tokens == 0) return BWD_OK;
+  if (!ids || !weight || !gamma || !beta || !y) return fail(BWD_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned_to(ids, 8) || !aligned_to(weight, 4) || !aligned_to(gamma, 4) || !aligned_to(beta, 4) ||
+      !aligned_to(y, 4) || !aligned_to(mean, 4) || !aligned_to(rstd, 4))
+    return fail(BWD_ERR_INVALID_ARG, "pointer not aligned to its element size");
+  EmbedDevice* d = nullptr;
+  if ((s = ensure_device(&d)) != BWD_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool fast = dim % 4 == 0 && dim <= kFastMaxDim && aligned16(weight) && aligned16(gamma) &&
+                    aligned16(beta) && aligned16(y);
+  if (fast) {
+    embed_fwd_kernel<<<grid_for(num_tokens, kFwdGroups, d->num_sms, d->occ_fwd), kGroup * kFwdGroups, 0, st>>>(
+        ids, num_tokens, weight, num_embeddings, static_cast<int>(dim), gamma, beta, eps, y, mean, rstd);
+    return check_launch("embed_fwd_kernel launch");
+  }
+  embed_fwd_slow_kernel<<<grid_for(num_tokens, kSlowGroups, d->num_sms, d->occ_slow_fwd), kGroup * kSlowGroups, 0,
+                          st>>>(ids, num_tokens, weight, num_embeddings, dim, gamma, beta, eps, y, mean, rstd);
+  return check_launch("embed_fwd_slow_kernel launch");
+}
+
+bwd_status bwd_embedding_backward(const int64_t* ids, int64_t num_tokens, const float* weight,
+                                  int64_t num_embeddings, int64_t dim, const float* gamma, const float* mean,
+                                  const float* rstd, const float* dy, float* dweight, float* dgamma, float* dbeta,
+                                  void* stream) {
+  bwd_status s = check_shape(num_embeddings, dim);
+  if (s != BWD_OK) return s;
+  if (num_tokens < 0) return fail(BWD_ERR_INVALID_ARG, "num_tokens < 0");
+  if (num_tokens > INT64_MAX / dim) return fail(BWD_ERR_INVALID_ARG, "num_tokens * dim overflows");
+  if (num_tokens == 0) return BWD_OK;
+  if (!ids || !weight || !gamma || !mean || !rstd || !dy || !dweight || !dgamma || !dbeta)
+    return fail(BWD_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned_to(ids, 8) || !aligned_to(weight, 4) || !aligned_to(gamma, 4) || !aligned_to(mean, 4) ||
+      !aligned_to(rstd, 4) || !aligned_to(dy, 4) || !aligned_to(dweight, 4) || !aligned_to(dgamma, 4) ||
+      !aligned_to(dbeta, 4))
+    return fail(BWD_ERR_INVALID_ARG, "pointer not aligned to its element size");
+  EmbedDevice* d = nullptr;
+  if ((s = ensure_device(&d)) != BWD_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool fast = dim % 4 == 0 && dim <= kFastMaxDim && aligned16(weight) && aligned16(gamma) &&
+                    aligned16(dy) && aligned16(dweight);
+  if (fast) {
+    const int smem = bwd_smem_bytes(static_cast<int>(dim));
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &occ, reinterpret_cast<const void*>(embed_bwd_kernel), kGroup * kBwdGroups, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    embed_bwd_kernel<<<grid_for(num_tokens, kBwdGroups, d->num_sms, occ > 0 ? occ : 1), kGroup * kBwdGroups, smem,
+                       st>>>(ids, num_tokens, weight, num_embeddings, static_cast<int>(dim), gamma, mean, rstd, dy,
+                             dweight, dgamma, dbeta);
+    return check_launch("embed_bwd_kernel launch");
+  }
+  embed_bwd_slow_kernel<<<grid_for(num_tokens, kSlowGroups, d->num_sms, d->occ_slow_bwd), kGroup * kSlowGroups, 0,
+                          st>>>(ids, num_tokens, weight, num_embeddings, dim, gamma, mean, rstd, dy, dweight, dgamma,
+                                dbeta);
+  return check_launch("embed_bwd_slow_kernel launch");
+}
+
+}  // extern "C"

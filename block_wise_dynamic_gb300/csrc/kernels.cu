@@ -39,6 +39,7 @@
 
 #include "bwd.h"
 #include "exact_div.cuh"
+#include "host_util.h"
 #include "tables.h"
 
 namespace {
@@ -576,7 +577,14 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
 // --------------------------------------------------------------------------
 // host side
 
+}  // namespace
+
+namespace bwd {
+namespace host {
+
+namespace {
 thread_local std::string t_last_error;
+}  // namespace
 
 bwd_status fail(bwd_status s, const char* fmt, ...) {
   char buf[512];
@@ -591,6 +599,25 @@ bwd_status fail(bwd_status s, const char* fmt, ...) {
 bwd_status cuda_fail(cudaError_t e, const char* what) {
   return fail(BWD_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
+
+bwd_status check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return BWD_OK;
+}
+
+const char* last_error() { return t_last_error.c_str(); }
+
+}  // namespace host
+}  // namespace bwd
+
+namespace {
+
+using bwd::host::aligned16;
+using bwd::host::aligned_to;
+using bwd::host::check_launch;
+using bwd::host::cuda_fail;
+using bwd::host::fail;
 
 struct DeviceState {
   bool ready = false;
@@ -659,7 +686,6 @@ bwd_status ensure_device(DeviceState** out) {
   return BWD_OK;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // CTAs for `blocks` quantization blocks when each CTA works on `per_cta` at a
 // time: enough to cover them, at most one full wave of resident CTAs.
@@ -669,11 +695,6 @@ int grid_for(int64_t blocks, int per_cta, const DeviceState& d, int occ) {
   return static_cast<int>(need < cap ? need : cap);
 }
 
-bwd_status check_launch(const char* what) {
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, what);
-  return BWD_OK;
-}
 
 bool valid_kind(bwd_map_kind k) { return k == BWD_MAP_SIGNED || k == BWD_MAP_UNSIGNED; }
 
@@ -736,7 +757,7 @@ const char* bwd_status_string(bwd_status s) {
   return "unknown status";
 }
 
-const char* bwd_last_error(void) { return t_last_error.c_str(); }
+const char* bwd_last_error(void) { return bwd::host::last_error(); }
 
 bwd_status bwd_init(void) {
   DeviceState* d = nullptr;
@@ -749,6 +770,7 @@ bwd_status bwd_quantize_blockwise(const float* x, int64_t n, bwd_map_kind kind, 
   if (!valid_kind(kind)) return fail(BWD_ERR_INVALID_ARG, "bad map kind %d", (int)kind);
   if (n == 0) return BWD_OK;
   if (!x || !codes || !absmax) return fail(BWD_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned_to(x, 4) || !aligned_to(absmax, 4)) return fail(BWD_ERR_INVALID_ARG, "fp32 pointer not 4-byte aligned");
   DeviceState* d = nullptr;
   bwd_status s = ensure_device(&d);
   if (s != BWD_OK) return s;
@@ -770,6 +792,7 @@ bwd_status bwd_dequantize_blockwise(const uint8_t* codes, const float* absmax, i
   if (!valid_kind(kind)) return fail(BWD_ERR_INVALID_ARG, "bad map kind %d", (int)kind);
   if (n == 0) return BWD_OK;
   if (!codes || !absmax || !y) return fail(BWD_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned_to(absmax, 4) || !aligned_to(y, 4)) return fail(BWD_ERR_INVALID_ARG, "fp32 pointer not 4-byte aligned");
   DeviceState* d = nullptr;
   bwd_status s = ensure_device(&d);
   if (s != BWD_OK) return s;
@@ -790,6 +813,8 @@ bwd_status bwd_state_init(uint8_t* m_codes, float* m_absmax, uint8_t* v_codes, f
   if (n < 0) return fail(BWD_ERR_INVALID_ARG, "n < 0");
   if (n == 0) return BWD_OK;
   if (!m_codes || !m_absmax || !v_codes || !v_absmax) return fail(BWD_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned_to(m_absmax, 4) || !aligned_to(v_absmax, 4))
+    return fail(BWD_ERR_INVALID_ARG, "fp32 pointer not 4-byte aligned");
   DeviceState* d = nullptr;
   bwd_status s = ensure_device(&d);
   if (s != BWD_OK) return s;
@@ -825,6 +850,9 @@ bwd_status step_multi(int32_t num_tensors, PP p, bwd_dtype p_dtype, const void* 
     if (n[i] < 0) return fail(BWD_ERR_INVALID_ARG, "tensor %d: n < 0", i);
     if (n[i] > 0 && (!p[i] || !g[i] || !m_codes[i] || !m_absmax[i] || !v_codes[i] || !v_absmax[i]))
       return fail(BWD_ERR_INVALID_ARG, "tensor %d: NULL pointer", i);
+    if (n[i] > 0 && (!aligned_to(p[i], p_dtype == BWD_BF16 ? 2 : 4) || !aligned_to(g[i], g_dtype == BWD_BF16 ? 2 : 4) ||
+                     !aligned_to(m_absmax[i], 4) || !aligned_to(v_absmax[i], 4)))
+      return fail(BWD_ERR_INVALID_ARG, "tensor %d: pointer not aligned to its element size", i);
     any_work = any_work || n[i] > 0;
   }
   if (!any_work) return BWD_OK;

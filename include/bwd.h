@@ -20,7 +20,9 @@
  *     the caller's next synchronisation, as for any CUDA work.
  *   - Arguments are checked on the host before anything is enqueued; a
  *     rejected call has no effect.  n == 0 is a successful no-op.
- *   - Any alignment is accepted.  16-byte aligned pointers (and, per tensor,
+ *   - Every pointer must be aligned to its element size (4 bytes for fp32,
+ *     2 for bf16, 8 for int64; BWD_ERR_INVALID_ARG otherwise).  Beyond that
+ *     any alignment is accepted: 16-byte aligned pointers (and, per tensor,
  *     full 2048-element blocks) take the vectorised path; other blocks take
  *     an element-wise path with identical results.
  *   - Input and output ranges must not overlap, except where an argument is
@@ -164,6 +166,62 @@ bwd_status bwd_adam8bit_step_multi_ex(int32_t num_tensors, void* const* p,
                                       uint8_t* const* v_codes,
                                       float* const* v_absmax, const int64_t* n,
                                       const bwd_adam_hparams* hp, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Stable embedding layer (section 二 / 稳定的词嵌入层): the embedding weight
+ * is initialised Xavier-uniform and a layer normalisation follows the
+ * lookup, so that the layer's output has variance close to 1.
+ *   weight : device fp32[V * D], row-major (row v = embedding of token v).
+ *   gamma, beta : device fp32[D], the normalisation's scale and shift.
+ *   ids    : device int64[T] token ids.  An id outside [0, V) is outside
+ *            the method: its output row is NaN (no access leaves the
+ *            weight) and the backward pass skips it.
+ * D a multiple of 4 and at most 4096 with 16-byte aligned weight, gamma,
+ * beta / dy, y / dweight takes the vectorised path; any other shape takes an
+ * element-wise path with the same arithmetic.  All fp32, eps as given.
+ * Errors: BWD_ERR_INVALID_ARG for V < 1, D < 1, T < 0, V * D or T * D
+ * overflowing int64, a NULL pointer, a non-finite or negative eps. */
+
+/* Xavier-uniform initialisation from caller-supplied random words:
+ * weight[i] = fp32((2 u_i - 1) * b), u_i = (words[i] >> 8) * 2^-24 and
+ * b = fp32(sqrt(6 / (V + D))) (Glorot's bound for fan-in D and fan-out V;
+ * 2 u - 1 is exact, so each weight takes one rounding).
+ *   words  : device uint32[V * D], e.g. from any uniform 32-bit generator.
+ *   weight : device fp32[V * D], written. */
+bwd_status bwd_embedding_init(const uint32_t* words, int64_t num_embeddings,
+                              int64_t dim, float* weight, void* stream);
+
+/* Host only: the bound b above, or -1 for V < 1 or D < 1. */
+float bwd_embedding_xavier_bound(int64_t num_embeddings, int64_t dim);
+
+/* Forward: for each token t with x = weight[ids[t]],
+ *   mean = sum(x) / D,  var = sum((x - mean)^2) / D,
+ *   rstd = 1 / sqrt(var + eps),  y = (x - mean) * rstd * gamma + beta.
+ *   y    : device fp32[T * D], written.
+ *   mean, rstd : device fp32[T], written (the backward pass reads them);
+ *          either may be NULL when no backward pass follows.
+ * Row statistics are reduced in a fixed order: results are deterministic. */
+bwd_status bwd_embedding_forward(const int64_t* ids, int64_t num_tokens,
+                                 const float* weight, int64_t num_embeddings,
+                                 int64_t dim, const float* gamma,
+                                 const float* beta, float eps, float* y,
+                                 float* mean, float* rstd, void* stream);
+
+/* Backward: with xhat = (x - mean) * rstd (mean, rstd from the forward call)
+ * and g = dy * gamma, per token
+ *   dx = rstd * (g - mean(g) - xhat * mean(g * xhat)),
+ * ACCUMULATED into the caller's buffers (zero them for a fresh gradient):
+ *   dweight[ids[t]] += dx   (device fp32[V * D]; repeated ids add up),
+ *   dgamma += sum_t dy * xhat,  dbeta += sum_t dy   (device fp32[D]).
+ *   dy : device fp32[T * D].
+ * The adds are atomic, so their order, and the last bits of dweight, dgamma
+ * and dbeta, may differ between runs. */
+bwd_status bwd_embedding_backward(const int64_t* ids, int64_t num_tokens,
+                                  const float* weight, int64_t num_embeddings,
+                                  int64_t dim, const float* gamma,
+                                  const float* mean, const float* rstd,
+                                  const float* dy, float* dweight,
+                                  float* dgamma, float* dbeta, void* stream);
 
 /* Static description of a status code. */
 const char* bwd_status_string(bwd_status status);

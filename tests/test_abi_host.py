@@ -110,3 +110,66 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     assert multi(2, arr, arr, 0, arr, arr, arr, arr, neg, ctypes.byref(hp), None) == 1
     assert multi(2, arr, nul, 0, arr, arr, arr, arr, ns, ctypes.byref(hp), None) == 1
     assert b"tensor 1" in lib.bwd_last_error()
+
+
+def test_embedding_xavier_bound_matches_oracle(lib):
+    from oracle import stable_embedding as se
+
+    for v, d in [(32000, 4096), (50304, 1024), (7, 5), (1, 1)]:
+        assert np.float32(lib.bwd_embedding_xavier_bound(v, d)).view(np.uint32) == se.xavier_bound(v, d).view(np.uint32)
+    assert lib.bwd_embedding_xavier_bound(0, 5) == -1.0
+    assert lib.bwd_embedding_xavier_bound(5, 0) == -1.0
+
+
+def test_embedding_bad_arguments_are_rejected_on_the_host(lib):
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: rejected first
+    init = lib.bwd_embedding_init
+    assert init(fake, 0, 4, fake, None) == 1
+    assert init(fake, 4, 0, fake, None) == 1
+    assert init(None, 4, 4, fake, None) == 1
+    assert init(fake, 2 ** 40, 2 ** 40, fake, None) == 1     # V * D overflows
+    fwd = lib.bwd_embedding_forward
+    ok = dict(ids=fake, t=10, w=fake, v=100, d=64, g=fake, b=fake, eps=1e-5, y=fake)
+
+    def f(**kw):
+        a = {**ok, **kw}
+        return fwd(a["ids"], a["t"], a["w"], a["v"], a["d"], a["g"], a["b"], a["eps"], a["y"], None, None, None)
+
+    assert f(t=-1) == 1
+    assert f(v=0) == 1
+    assert f(d=0) == 1
+    assert f(eps=-1.0) == 1
+    assert f(eps=float("inf")) == 1
+    assert f(eps=float("nan")) == 1
+    assert f(ids=None) == 1 and f(w=None) == 1 and f(g=None) == 1 and f(b=None) == 1 and f(y=None) == 1
+    assert f(t=2 ** 62, d=64) == 1                          # T * D overflows
+    assert f(t=0, ids=None, w=None, y=None) == 0            # no tokens: no-op without a device
+    bwd = lib.bwd_embedding_backward
+    args = [fake, 10, fake, 100, 64, fake, fake, fake, fake, fake, fake, fake, None]
+    for i in (0, 2, 5, 6, 7, 8, 9, 10, 11):                 # every pointer argument
+        a = list(args)
+        a[i] = None
+        assert bwd(*a) == 1
+    a = list(args)
+    a[1] = -5
+    assert bwd(*a) == 1
+    a = [None] * 13
+    a[1], a[3], a[4] = 0, 100, 64
+    assert bwd(*a) == 0
+
+
+def test_pointers_misaligned_for_their_element_size_are_rejected(lib):
+    from block_wise_dynamic_gb300._abi import AdamHParams
+
+    ok, odd = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1001)
+    assert lib.bwd_quantize_blockwise(odd, 10, 0, ok, ok, None) == 1
+    assert b"aligned" in lib.bwd_last_error()
+    assert lib.bwd_dequantize_blockwise(ok, ok, 10, 0, odd, None) == 1
+    assert lib.bwd_state_init(ok, odd, ok, ok, 10, None) == 1
+    hp = AdamHParams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1)
+    assert lib.bwd_adam8bit_step(odd, ok, 0, ok, ok, ok, ok, 10, ctypes.byref(hp), None) == 1
+    two = ctypes.c_void_p(0x1002)  # fine for bf16, not for fp32
+    assert lib.bwd_adam8bit_step(ok, two, 0, ok, ok, ok, ok, 10, ctypes.byref(hp), None) == 1
+    assert lib.bwd_embedding_forward(ctypes.c_void_p(0x1004), 10, ok, 100, 64, ok, ok, 1e-5, ok, None, None,
+                                     None) == 1
+    assert lib.bwd_embedding_init(ok, 4, 4, two, None) == 1
