@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llama2_7b",
-                    choices=["llama2_7b", "gpt_350m", "ragged_2000", "adam_1m", "quant_2p28"])
+                    choices=["llama2_7b", "gpt_350m", "ragged_2000", "adam_1m", "quant_2p28", "embed_7b"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--param-dtype", default="f32", choices=["f32", "bf16"],
                     help="parameter storage (bf16: widened for the update, rounded back)")
@@ -308,11 +308,18 @@ def run_reference(args):
     world, rank, _ = dist_info()
     if rank != 0:
         return
+    metric = METRIC
     if args.workload == "quant_2p28":
         n = 2 ** 20
         rate, dt, procs = oracle_pool_rate("quant", n, steps=args.steps, warm=args.warmup)
         unit = "elements/s"
         what = f"each step: the oracle's four passes on {n} elements in each of {procs} processes"
+    elif args.workload == "embed_7b":
+        n, procs, metric = 1024, 1, EMBED_METRIC
+        rate, dt = oracle_embed_rate(n, steps=args.steps, warm=args.warmup)
+        unit = "tokens/s"
+        what = (f"each step: the oracle's forward + backward on {n} tokens of the embed_7b workload "
+                f"(full 32000 x 4096 weight), one process")
     else:
         n = 1024 * 2048
         rate, dt, procs = oracle_pool_rate("adam", n, steps=args.steps, warm=args.warmup)
@@ -320,7 +327,7 @@ def run_reference(args):
         what = (f"each step: the oracle's 8-bit Adam step on {n} params (1024 blocks) "
                 f"of the {args.workload} distributions in each of {procs} processes")
     line = {
-        "impl": "reference", "metric": METRIC, "value": rate, "unit": unit, "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric, "value": rate, "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
@@ -626,12 +633,242 @@ def run_quant(args):
         torch.distributed.destroy_process_group()
 
 
+# --------------------------------------------------------------------------
+# the stable embedding layer (lookup + LayerNorm, forward and backward)
+
+EMBED_METRIC = "stable embedding (lookup + LayerNorm) forward+backward tokens/sec and achieved HBM GB/s"
+
+
+def embed_bytes(v: int, d: int, t: int, unique: int) -> dict:
+    """Minimal DRAM bytes of each pass: every distinct row read once, y and
+    dy streamed, each touched gradient row read and written once, ids and
+    per-token statistics (gamma, beta, dgamma, dbeta are negligible)."""
+    fwd = 4 * d * unique + 4 * d * t + 8 * t + 8 * t
+    bwd = 4 * d * t + 4 * d * unique + 8 * d * unique + 8 * t + 8 * t
+    return {"forward": fwd, "backward": bwd}
+
+
+def embed_traffic():
+    """DRAM bytes per launch of the two embedding kernels from the committed
+    ncu summary, valid only while the kernel source is the one profiled."""
+    src = os.path.join(ROOT, "block_wise_dynamic_gb300", "csrc", "embedding.cu")
+    prof = os.path.join(ROOT, "profiles", "embed_kernels_embed_7b.md")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        text = open(prof).read()
+    except OSError:
+        return None
+    if sha not in text:
+        return None
+    out = {}
+    for name in ("forward", "backward"):
+        for line in text.splitlines():
+            if line.startswith(f"- dram bytes per {name} launch:"):
+                out[name] = float(line.split(":")[1])
+    return out or None
+
+
+def oracle_embed_rate(tokens: int, steps: int, warm: int = 0):
+    """Tokens/s of the oracle's forward + backward on `tokens` tokens of the
+    embed_7b workload (the full 32,000 x 4,096 weight), one process."""
+    import numpy as np
+
+    from oracle import stable_embedding as se
+    from block_wise_dynamic_gb300 import workloads as W
+
+    v, d, _ = W.EMBED_7B
+    w = se.init_weight(W.random_words(v * d, seed=1).numpy().view(np.uint32), v, d)
+    ids = W.token_ids(tokens, v, seed=0).numpy()
+    gamma, beta = np.ones(d, np.float32), np.zeros(d, np.float32)
+    dy = W.gen_normal(tokens * d, 1.0, seed=61).numpy().reshape(tokens, d).astype(np.float64)
+
+    def step():
+        se.forward(ids, w, gamma, beta)
+        se.backward(ids, w, gamma, dy)
+
+    for _ in range(warm):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = time.perf_counter() - t0
+    return tokens * steps / dt, dt
+
+
+def run_embed(args):
+    """Forward + backward of the stable embedding layer on Llama-2-7B's
+    embedding (32,000 x 4,096) with 4 x 4,096 Zipf-distributed tokens."""
+    import numpy as np
+    import torch
+
+    from block_wise_dynamic_gb300 import embedding as E
+    from block_wise_dynamic_gb300 import workloads as W
+
+    world, rank, local = dist_info()
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    v, d, t = W.EMBED_7B
+    w = torch.empty(v, d, dtype=torch.float32, device=dev)
+    E.init_weight(w, W.random_words(v * d, seed=1 + rank).to(dev))
+    gamma = torch.ones(d, dtype=torch.float32, device=dev)
+    beta = torch.zeros(d, dtype=torch.float32, device=dev)
+    ids_h = W.token_ids(t, v, seed=rank)
+    unique = int(torch.unique(ids_h).numel())
+    ids = ids_h.to(dev)
+    dy = W.gen_normal(t * d, 1.0, seed=61 + rank, device=dev).view(t, d)
+    dw = torch.zeros_like(w)
+    dg = torch.zeros_like(gamma)
+    db = torch.zeros_like(gamma)
+    y = torch.empty(t, d, dtype=torch.float32, device=dev)
+    mean = torch.empty(t, dtype=torch.float32, device=dev)
+    rstd = torch.empty(t, dtype=torch.float32, device=dev)
+    lib = E._lib
+    st_h = torch.cuda.current_stream(dev).cuda_stream
+    stream = torch.cuda.current_stream(dev)
+
+    from block_wise_dynamic_gb300 import _abi
+
+    def fwd():
+        _abi.check(lib.bwd_embedding_forward(ids.data_ptr(), t, w.data_ptr(), v, d, gamma.data_ptr(),
+                                             beta.data_ptr(), E.EPS, y.data_ptr(), mean.data_ptr(), rstd.data_ptr(),
+                                             st_h), "bwd_embedding_forward")
+
+    def bwd():
+        _abi.check(lib.bwd_embedding_backward(ids.data_ptr(), t, w.data_ptr(), v, d, gamma.data_ptr(),
+                                              mean.data_ptr(), rstd.data_ptr(), dy.data_ptr(), dw.data_ptr(),
+                                              dg.data_ptr(), db.data_ptr(), st_h), "bwd_embedding_backward")
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(dev)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
+          for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    c0 = time.perf_counter()
+    e0.record(stream)
+    for k in range(args.steps):
+        for j, f in enumerate((fwd, bwd)):
+            ev[k][j][0].record(stream)
+            f()
+            ev[k][j][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    c1 = time.perf_counter()
+    clocks.stop()
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    nbytes = embed_bytes(v, d, t, unique)
+    per = {}
+    for j, name in enumerate(("forward", "backward")):
+        ms = statistics.fmean(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(args.steps))
+        per[name] = {"ms": ms, "tokens_per_s": t / (ms / 1e3), "gbs": nbytes[name] / (ms / 1e3) / 1e9,
+                     "bytes": nbytes[name]}
+
+    # end to end through the public API: the step's token ids and dL/dy
+    # arrive from pinned host memory, dgamma and dbeta go back to it
+    e2e = None
+    if args.e2e_steps > 0:
+        ids_p = torch.empty(t, dtype=torch.int64, pin_memory=True)
+        ids_p.copy_(ids_h)
+        dy_p = torch.empty(t, d, dtype=torch.float32, pin_memory=True)
+        dy_p.copy_(dy)
+        out_p = torch.empty(2, d, dtype=torch.float32, pin_memory=True)
+
+        def e2e_step():
+            ids.copy_(ids_p, non_blocking=True)
+            dy.copy_(dy_p, non_blocking=True)
+            fwd()
+            bwd()
+            out_p[0].copy_(dg, non_blocking=True)
+            out_p[1].copy_(db, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        f0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(f0.elapsed_time(f1), dev)
+        e2e = {"value": world * t * args.e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": t * 8 + t * d * 4, "d2h_bytes_per_step": 2 * d * 4,
+               "steps": args.e2e_steps,
+               "what": "per step: token ids and dL/dy H2D from pinned host memory, forward, backward, "
+                       "dgamma and dbeta D2H into pinned host memory"}
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    dom = max(per, key=lambda k: per[k]["ms"])
+    peak, peak_kind = measured_peak()
+    achieved = per[dom]["gbs"]
+    tr = embed_traffic()
+    line = {
+        "metric": EMBED_METRIC,
+        "value": world * t * args.steps / (elapsed_ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": "embed_7b",
+            "num_embeddings": v, "dim": d, "tokens": t, "distinct_tokens": unique,
+            "ids": "Zipf frequencies p(rank k) ~ 1/(k+1), ranks permuted (seed = rank)",
+            "grad_accumulation": "dweight, dgamma, dbeta accumulate across steps (not zeroed in the timed region)",
+            "l2": f"{(nbytes['forward'] + nbytes['backward']) / 1e6:.0f} MB of minimal DRAM traffic per step vs "
+                  f"{L2_BYTES / 2**20:.0f} MiB L2; repeated rows hit L2 by design, no flush",
+            "parallelism": f"replica per GPU x{world}",
+        },
+        "passes": per,
+        "hbm_gbs": (nbytes["forward"] + nbytes["backward"]) / (elapsed_ms / args.steps / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "embed_bwd_kernel" if dom == "backward" else "embed_fwd_kernel",
+                     "achieved": achieved, "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None if tr is None or dom not in tr else tr[dom],
+                     "bytes_per_launch": nbytes[dom], "mean_launch_ms": per[dom]["ms"]},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(c0, c1),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        n = 1024
+        rate, dt = oracle_embed_rate(n, steps=2)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"2 steps of the oracle's forward + backward on {n} tokens of the same "
+                                          f"workload (full {v} x {d} weight), {dt:.1f} s, one process (each worker "
+                                          f"would hold the weight and a binary64 gradient, ~1.5 GB)"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "quant_2p28":
         run_quant(args)
+    elif args.workload == "embed_7b":
+        run_embed(args)
     else:
         run_ours(args)
 
