@@ -67,10 +67,25 @@ __device__ bwd::Tables g_tables;  // immutable after the first upload per device
 // --------------------------------------------------------------------------
 // device helpers
 
+// Max over a warp of non-negative values: their bit patterns order like the
+// values, so one unsigned integer reduction (redux.sync) does it.  Every
+// caller passes magnitudes (|m|, v >= 0, |x|); a NaN, outside the method,
+// wins here where fmaxf would drop it, and still indexes nothing out of
+// bounds downstream.
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
+}
+
+// Three-input max (sm_100 and later); the .abs form takes magnitudes.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float max3abs(float a, float b, float c) {
+  float d;
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // Named barrier of one 128-thread group (barrier 0 is __syncthreads).
@@ -200,7 +215,8 @@ __device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, 
     w[k] = __byte_perm(__byte_perm(c[4 * k], c[4 * k + 1], 0x0073), __byte_perm(c[4 * k + 2], c[4 * k + 3], 0x0073), 0x5410);
 }
 
-// Max over the 128 threads of a group; every thread gets the result.
+// Max over the 128 threads of a group of non-negative values; every thread
+// gets the result.
 // `red` is this group's [2 parities][values][4 warps] scratch.
 template <int kVals>
 __device__ __forceinline__ void group_max(float (&v)[kVals], float* red, int parity, int group, int t) {
@@ -265,7 +281,7 @@ quantize_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ co
     }
     float mx[1] = {0.0f};
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) mx[0] = fmaxf(mx[0], fabsf(v[j]));
+    for (int j = 0; j < kPer; j += 2) mx[0] = max3abs(mx[0], v[j], v[j + 1]);
     group_max<1>(mx, s_red[group], it & 1, group, t);
     const float am = mx[0];
 
@@ -522,8 +538,8 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
       const float2 rc = make_float2(rcp_approx(den.x), rcp_approx(den.y));
       const float2 pp = bwd::fma2(bwd::mul2(nstep2, mm), rc, bwd::mul2(make_float2(p[j], p[j + 1]), decay2));
       p[j] = pp.x; p[j + 1] = pp.y;
-      mx[0] = fmaxf(mx[0], fmaxf(fabsf(mm.x), fabsf(mm.y)));
-      mx[1] = fmaxf(mx[1], fmaxf(vv.x, vv.y));
+      mx[0] = max3abs(mx[0], mm.x, mm.y);
+      mx[1] = max3(mx[1], vv.x, vv.y);
     }
     if (vec) {
 #pragma unroll
