@@ -9,15 +9,18 @@
 // stores them quantized again.
 //
 // Work decomposition.  A group of 128 threads owns one 2048-element block at a
-// time; a CTA holds two groups (four in the standalone quantizer, which
-// needs fewer registers) and the groups walk the blocks with a grid stride
-// (grid = SMs x resident CTAs).  Thread t of a group owns the 16
-// elements 4 t + 512 k + j (k, j < 4) of its block ("quads" of 4 elements,
-// 4 x 128 = 512 elements apart), so every warp-wide load or store touches one
-// contiguous span (512 B of fp32, 256 B of bf16, 128 B of codes) and is fully
-// coalesced.  The block absmax is a warp shuffle
-// reduction and a pass over the group's four warps through shared memory,
-// synchronised by a named barrier per group.  The maps, thresholds and the
+// time and the groups walk the blocks with a grid stride (grid = SMs x
+// resident CTAs).  The fused step runs one 768-thread CTA of six groups per
+// SM (80 registers x 768 threads fill the register file), so the code tables
+// sit in shared memory once per SM and leave the rest of the unified array
+// to L1 for the loads in flight (three 256-thread CTAs per SM, each with its
+// own copy, ran 4% slower); the standalone quantizer runs two CTAs of four
+// groups.  Thread t of a group owns the 16 elements 4 t + 512 k + j (k, j < 4)
+// of its block ("quads" of 4 elements, 4 x 128 = 512 elements apart), so
+// every warp-wide load or store touches one contiguous span (512 B of fp32,
+// 256 B of bf16, 128 B of codes) and is fully coalesced.  The block absmax is
+// a warp reduction and a pass over the group's four warps through shared
+// memory, synchronised by a named barrier per group.  The maps and the
 // bucket entries (tables.h) are copied once per CTA into dynamic shared memory.
 //
 // Exactness.  Every operation that decides a code is IEEE binary32 with
@@ -51,8 +54,8 @@ constexpr int kPer = BWD_BLOCK / kGroup;      // 16 elements per thread
 constexpr int kQuads = kPer / 4;              // 4-element quads per thread
 constexpr int kSpan = 4 * kGroup;             // elements between a thread's quads
 constexpr int kGroupWarps = kGroup / 32;      // 4
-constexpr int kGroups = 2;                    // blocks in flight per CTA (Adam)
-constexpr int kCta = kGroup * kGroups;        // 256 threads
+constexpr int kGroups = 6;                    // blocks in flight per CTA (Adam), one CTA per SM
+constexpr int kCta = kGroup * kGroups;        // 768 threads
 constexpr int kQGroups = 4;                   // blocks in flight per CTA (quantize)
 constexpr int kQCta = kGroup * kQGroups;      // 512 threads
 constexpr int kDeqThreads = 256;              // dequantize: 8 elements per thread
@@ -423,7 +426,7 @@ __device__ __forceinline__ uint32_t bf16_bits(float x) {
 // kBf16: gradient type; kPBf16: parameter type (bf16 parameters are widened
 // for the update and rounded back to bf16 on store).
 template <bool kBf16, bool kPBf16>
-__global__ void __launch_bounds__(kCta, 3)
+__global__ void __launch_bounds__(kCta, 1)
 adam8bit_kernel(const __grid_constant__ AdamArgs args) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   bwd::Tables& tab = *reinterpret_cast<bwd::Tables*>(smem_raw);
