@@ -26,6 +26,7 @@ __all__ = [
     "num_blocks",
     "build_map",
     "init",
+    "check_device",
     "quantize_blockwise",
     "dequantize_blockwise",
     "state_init",
@@ -90,6 +91,14 @@ def build_map(kind="signed"):
     t = np.empty(255, np.float32)
     _abi.check(_lib.bwd_build_map(_kind(kind), m.ctypes.data, t.ctypes.data), "bwd_build_map")
     return m, t
+
+
+def check_device(device=None, stream=None) -> None:
+    """Wait for the stream and raise BwdError if a bounded wait inside one of
+    the library's kernels gave up since the last check (the flag is cleared)."""
+    dev = torch.device(device if device is not None else torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        _abi.check(_lib.bwd_check_device(_stream_handle(dev, stream)), "bwd_check_device")
 
 
 def init(device=None) -> None:

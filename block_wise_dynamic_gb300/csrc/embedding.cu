@@ -9,27 +9,33 @@
 // and a learnable scale gamma and shift beta; the backward pass is the
 // gradient of that map, accumulated into the weight rows of the tokens.
 //
-// Work decomposition.  A group of 128 threads owns one token (one row of D
-// fp32 values) at a time and walks the tokens with a grid stride.  On the
-// fast path (D a multiple of 4 and at most 4096, every row pointer 16-byte
-// aligned) thread t of a group holds the float4 chunks t, t + 128, ... of
-// the row in registers, so a row is read from HBM once: every warp access is
-// one contiguous 512-byte span.  Row statistics are sums over the group
-// (warp shuffles, then the group's four warp partials through shared memory
-// in a fixed order, so results do not depend on scheduling).  Forward: mean,
-// then the centred sum of squares from the registers (two passes over the
-// registers, one over memory), then y = (x - mean) rstd gamma + beta.
-// Backward: xhat from the saved mean and rstd, the two sums of
-// g = dy gamma and g xhat, dx = rstd (g - mean(g) - xhat mean(g xhat))
-// added into the weight row with vector reductions (red.global.add.v4.f32;
-// tokens repeat, so the adds are atomic), while each thread accumulates
-// dgamma and dbeta for its own columns in shared memory; each CTA adds its
-// partials into dgamma and dbeta once at the end.  On the fast path a few
-// threads of each group ask L2 (cp.async.bulk.prefetch.L2) for the rows of
-// the group's next token while the current one is processed: the backward
-// pass ran 0.19 ms without it, 0.14 ms with it on the 32,000 x 4,096 /
-// 16,384-token case.  Other shapes take a per-element path with the same
-// arithmetic.
+// Work decomposition.  Forward: a group of 128 threads owns one token (one
+// row of D fp32 values) at a time and walks the tokens with a grid stride.
+// On the fast path (D a multiple of 4 and at most 4096, every row pointer
+// 16-byte aligned) thread t of a group holds the float4 chunks t, t + 128,
+// ... of the row in registers, so a row is read from HBM once: every warp
+// access is one contiguous 512-byte span.  Row statistics are sums over the
+// group (warp shuffles, then the group's warp partials through shared memory
+// in a fixed order, so results do not depend on scheduling): mean, then the
+// centred sum of squares from the registers, then
+// y = (x - mean) rstd gamma + beta.  Thread 0 asks L2 for the group's next
+// row meanwhile (cp.async.bulk.prefetch.L2).
+//
+// Backward, fast path: one 768-thread CTA per SM, three groups of 256
+// threads.  Thread 0 of a group copies the weight row and the dy row of the
+// group's NEXT token into the second of two shared-memory buffers
+// (cp.async.bulk, completion counted on one mbarrier per buffer) while the
+// group works on the current token from the first: xhat from the saved mean
+// and rstd, the two sums of g = dy gamma and g xhat, then
+// dx = rstd (g - mean(g) - xhat mean(g xhat)) added into the weight row with
+// vector reductions (red.global.add.v4.f32; tokens repeat, so the adds are
+// atomic).  The rows live in shared memory, not registers, so the loads of
+// the next token overlap all of the current one's arithmetic; each thread
+// keeps dgamma and dbeta for its own columns in registers, and each CTA adds
+// the sum of its groups' partials into dgamma and dbeta once at the end
+// (0.144 ms with the rows in registers and an L2 prefetch, 0.115 ms staged,
+// on the 32,000 x 4,096 / 16,384-token case).  Other shapes take a
+// per-element path with the same arithmetic.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -52,7 +58,6 @@ constexpr int kGroupWarps = kGroup / 32;          // 4
 constexpr int kChunks = 8;                        // float4 chunks per thread on the fast path
 constexpr int kFastMaxDim = kGroup * 4 * kChunks; // 4096
 constexpr int kFwdGroups = 2;                     // forward CTA: 256 threads
-constexpr int kBwdGroups = 2;                     // backward CTA: 256 threads
 constexpr int kSlowGroups = 2;                    // per-element path: 256 threads
 constexpr int kInitThreads = 256;
 constexpr int kMaxDevices = 64;
@@ -242,107 +247,6 @@ embed_fwd_slow_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const
 // backward: dweight[id] += dx, dgamma += dy xhat, dbeta += dy (accumulated).
 // Tokens whose id lies outside [0, V) are skipped.
 
-__host__ __device__ constexpr int bwd_smem_bytes(int dim) { return kBwdGroups * 2 * dim * 4; }
-
-__global__ void __launch_bounds__(kGroup * kBwdGroups, 2)
-embed_bwd_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const float* __restrict__ w, int64_t vocab,
-                 int dim, const float* __restrict__ gamma, const float* __restrict__ mean,
-                 const float* __restrict__ rstd, const float* __restrict__ dy, float* __restrict__ dw,
-                 float* __restrict__ dgamma, float* __restrict__ dbeta) {
-  extern __shared__ __align__(16) float s_part[];  // [group][dgamma | dbeta][dim]
-  __shared__ __align__(16) float s_red[kBwdGroups][2 * 2 * kGroupWarps];
-  const int group = threadIdx.x / kGroup, t = threadIdx.x % kGroup;
-  const int nch = dim >> 2;
-  const float fdim = static_cast<float>(dim);
-  float* const pg = s_part + static_cast<int64_t>(group) * 2 * dim;
-  float* const pb = pg + dim;
-#pragma unroll
-  for (int k = 0; k < kChunks; ++k) {
-    const int c = t + kGroup * k;
-    if (c < nch) {
-      *reinterpret_cast<float4*>(pg + 4 * c) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      *reinterpret_cast<float4*>(pb + 4 * c) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    }
-  }
-  int slot = 0;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kBwdGroups;
-  for (int64_t tok = static_cast<int64_t>(blockIdx.x) * kBwdGroups + group; tok < num_tokens; tok += stride) {
-    const int64_t id = ids[tok];
-    if (id < 0 || id >= vocab) continue;  // the whole group skips together
-    const float mu = mean[tok], r = rstd[tok];
-    const float* row = w + id * static_cast<int64_t>(dim);
-    const float* drow = dy + tok * static_cast<int64_t>(dim);
-    if (t < 2 && tok + stride < num_tokens) {  // L2 fetches the group's next dy and weight rows meanwhile
-      const int64_t nt = tok + stride, nid = ids[nt];
-      prefetch_l2(t == 0 ? static_cast<const void*>(dy + nt * static_cast<int64_t>(dim))
-                         : static_cast<const void*>(w + ((nid >= 0 && nid < vocab) ? nid : 0) * static_cast<int64_t>(dim)),
-                  static_cast<uint32_t>(dim * 4));
-    }
-    float4 xh[kChunks], d[kChunks];
-    float s[2] = {0.0f, 0.0f};
-#pragma unroll
-    for (int k = 0; k < kChunks; ++k) {
-      const int c = t + kGroup * k;
-      if (c < nch) {
-        const float4 x = ld4(row + 4 * c);
-        d[k] = __ldcs(reinterpret_cast<const float4*>(drow + 4 * c));
-        const float4 g = ldg4(gamma + 4 * c);
-        xh[k] = make_float4(__fmul_rn(__fsub_rn(x.x, mu), r), __fmul_rn(__fsub_rn(x.y, mu), r),
-                            __fmul_rn(__fsub_rn(x.z, mu), r), __fmul_rn(__fsub_rn(x.w, mu), r));
-        const float4 gg = make_float4(__fmul_rn(d[k].x, g.x), __fmul_rn(d[k].y, g.y), __fmul_rn(d[k].z, g.z),
-                                      __fmul_rn(d[k].w, g.w));
-        s[0] = __fadd_rn(s[0], __fadd_rn(__fadd_rn(gg.x, gg.y), __fadd_rn(gg.z, gg.w)));
-        s[1] = __fadd_rn(s[1], __fadd_rn(__fadd_rn(__fmul_rn(gg.x, xh[k].x), __fmul_rn(gg.y, xh[k].y)),
-                                         __fadd_rn(__fmul_rn(gg.z, xh[k].z), __fmul_rn(gg.w, xh[k].w))));
-      } else {
-        xh[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        d[k] = xh[k];
-      }
-    }
-    group_sum<2>(s, s_red[group], slot, group, t);
-    slot ^= 1;
-    const float m1 = __fdiv_rn(s[0], fdim), m2 = __fdiv_rn(s[1], fdim);
-    float* dwrow = dw + id * static_cast<int64_t>(dim);
-#pragma unroll
-    for (int k = 0; k < kChunks; ++k) {
-      const int c = t + kGroup * k;
-      if (c < nch) {
-        const float4 g = ldg4(gamma + 4 * c);
-        float4 dx;
-        dx.x = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d[k].x, g.x), m1), __fmul_rn(xh[k].x, m2)));
-        dx.y = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d[k].y, g.y), m1), __fmul_rn(xh[k].y, m2)));
-        dx.z = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d[k].z, g.z), m1), __fmul_rn(xh[k].z, m2)));
-        dx.w = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d[k].w, g.w), m1), __fmul_rn(xh[k].w, m2)));
-        red_add4(dwrow + 4 * c, dx);
-        float4 a = *reinterpret_cast<float4*>(pg + 4 * c);
-        a.x = __fadd_rn(a.x, __fmul_rn(d[k].x, xh[k].x));
-        a.y = __fadd_rn(a.y, __fmul_rn(d[k].y, xh[k].y));
-        a.z = __fadd_rn(a.z, __fmul_rn(d[k].z, xh[k].z));
-        a.w = __fadd_rn(a.w, __fmul_rn(d[k].w, xh[k].w));
-        *reinterpret_cast<float4*>(pg + 4 * c) = a;
-        float4 b = *reinterpret_cast<float4*>(pb + 4 * c);
-        b.x = __fadd_rn(b.x, d[k].x);
-        b.y = __fadd_rn(b.y, d[k].y);
-        b.z = __fadd_rn(b.z, d[k].z);
-        b.w = __fadd_rn(b.w, d[k].w);
-        *reinterpret_cast<float4*>(pb + 4 * c) = b;
-      }
-    }
-  }
-  // the CTA's partials, summed over its groups in a fixed order, go out once
-  __syncthreads();
-  for (int i = threadIdx.x; i < dim; i += blockDim.x) {
-    float a = 0.0f, b = 0.0f;
-#pragma unroll
-    for (int gi = 0; gi < kBwdGroups; ++gi) {
-      a = __fadd_rn(a, s_part[static_cast<int64_t>(gi) * 2 * dim + i]);
-      b = __fadd_rn(b, s_part[static_cast<int64_t>(gi) * 2 * dim + dim + i]);
-    }
-    atomicAdd(dgamma + i, a);
-    atomicAdd(dbeta + i, b);
-  }
-}
-
 __global__ void __launch_bounds__(kGroup * kSlowGroups)
 embed_bwd_slow_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const float* __restrict__ w,
                       int64_t vocab, int64_t dim, const float* __restrict__ gamma, const float* __restrict__ mean,
@@ -380,6 +284,227 @@ embed_bwd_slow_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const
 }
 
 // --------------------------------------------------------------------------
+// backward, fast path: rows staged in shared memory by bulk copies
+//
+// Every wait here is bounded: after about a second (or 2^24 polls) it gives
+// up, sets g_embed_fault (read and cleared by bwd_check_device), and the
+// group leaves its loop at the next group barrier after letting its copy in
+// flight land, again with a bounded wait.
+__device__ unsigned int g_embed_fault;  // set when a bounded wait gives up
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}"
+               ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
+  uint32_t done;
+  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+               " selp.u32 %0, 1, 0, p;\n}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < (1u << 24); ++i) {
+    if (mbar_try(a, parity)) return true;
+    if (global_ns() - t0 > 1000000000ull) return false;
+  }
+  return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  return mbar_try(a, parity) || mbar_wait_slow(a, parity);
+}
+
+constexpr int kSG = 256;                 // threads per token, staged backward
+constexpr int kSGWarps = kSG / 32;
+constexpr int kSGroups = 3;              // groups per CTA, one CTA per SM
+constexpr int kSChunks = kFastMaxDim / (4 * kSG);  // 4 float4 chunks per thread
+
+__host__ __device__ constexpr int staged_smem_bytes(int dim) { return kSGroups * 2 * 2 * dim * 4; }
+
+__device__ __forceinline__ void group_sync256(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "n"(kSG) : "memory");
+}
+
+template <int kVals>
+__device__ __forceinline__ void group_sum256(float (&v)[kVals], float* red, int slot, int group, int t) {
+  const int lane = t & 31, warp = t >> 5;
+#pragma unroll
+  for (int i = 0; i < kVals; ++i) v[i] = warp_sum(v[i]);
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < kVals; ++i) red[(slot * kVals + i) * kSGWarps + warp] = v[i];
+  }
+  group_sync256(group);
+#pragma unroll
+  for (int i = 0; i < kVals; ++i) {
+    const float4 a = *reinterpret_cast<const float4*>(&red[(slot * kVals + i) * kSGWarps]);
+    const float4 b = *reinterpret_cast<const float4*>(&red[(slot * kVals + i) * kSGWarps + 4]);
+    v[i] = __fadd_rn(__fadd_rn(__fadd_rn(a.x, a.y), __fadd_rn(a.z, a.w)), __fadd_rn(__fadd_rn(b.x, b.y), __fadd_rn(b.z, b.w)));
+  }
+}
+
+// Backward with the rows staged in shared memory: thread 0 of each group
+// copies the next token's weight and dy rows (cp.async.bulk, one mbarrier
+// per buffer) while the group works on the current token from the other
+// buffer; dgamma / dbeta partials stay in registers.
+__global__ void __launch_bounds__(kSG * kSGroups, 1)
+embed_bwd_staged_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const float* __restrict__ w, int64_t vocab,
+                        int dim, const float* __restrict__ gamma, const float* __restrict__ mean,
+                        const float* __restrict__ rstd, const float* __restrict__ dy, float* __restrict__ dw,
+                        float* __restrict__ dgamma, float* __restrict__ dbeta) {
+  extern __shared__ __align__(128) float s_buf[];  // [group][buffer][x | dy][dim]
+  __shared__ __align__(16) float s_red[kSGroups][2 * 2 * kSGWarps];
+  __shared__ __align__(8) uint64_t s_full[kSGroups][2];
+  __shared__ int s_abort[kSGroups];
+  const int group = threadIdx.x / kSG, t = threadIdx.x % kSG;
+  const int nch = dim >> 2;
+  const float fdim = static_cast<float>(dim);
+  const uint32_t row_bytes = static_cast<uint32_t>(dim) * 4u;
+  float* const gbuf = s_buf + static_cast<int64_t>(group) * 4 * dim;
+  if (t == 0) {
+    mbar_init(&s_full[group][0], 1);
+    mbar_init(&s_full[group][1], 1);
+    s_abort[group] = 0;
+  }
+  __syncthreads();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kSGroups;
+  const int64_t tok0 = static_cast<int64_t>(blockIdx.x) * kSGroups + group;
+  // copies of token `tok` into buffer `b` (nothing for an id outside [0, V))
+  auto issue = [&](int64_t tok, int b) {
+    const int64_t id = ids[tok];
+    if (id < 0 || id >= vocab) return;
+    uint64_t* bar = &s_full[group][b];
+    mbar_expect_tx(bar, 2u * row_bytes);
+    bulk_g2s(gbuf + b * 2 * dim, w + id * static_cast<int64_t>(dim), row_bytes, bar);
+    bulk_g2s(gbuf + b * 2 * dim + dim, dy + tok * static_cast<int64_t>(dim), row_bytes, bar);
+  };
+  if (t == 0 && tok0 < num_tokens) issue(tok0, 0);
+  float4 pg[kSChunks], pb[kSChunks];
+#pragma unroll
+  for (int k = 0; k < kSChunks; ++k) pg[k] = pb[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  uint32_t phase = 0;  // bit b: parity of buffer b's next phase
+  int slot = 0;
+  int pending = -1;    // buffer with copies issued and not yet waited for
+  if (tok0 < num_tokens) {
+    const int64_t id0 = ids[tok0];
+    if (id0 >= 0 && id0 < vocab) pending = 0;
+  }
+  int it = 0;
+  for (int64_t tok = tok0; tok < num_tokens; tok += stride, ++it) {
+    const int b = it & 1;
+    group_sync256(group);  // every thread is done with the other buffer
+    if (s_abort[group]) break;
+    if (t == 0 && tok + stride < num_tokens) issue(tok + stride, b ^ 1);
+    const int64_t id = ids[tok];
+    if (id < 0 || id >= vocab) continue;  // the whole group skips together
+    const bool ok = mbar_wait(&s_full[group][b], (phase >> b) & 1u);
+    phase ^= 1u << b;
+    if (!ok) {
+      atomicOr(&g_embed_fault, 1u);
+      s_abort[group] = 1;
+    }
+    {
+      const int64_t nx = tok + stride;
+      pending = -1;
+      if (nx < num_tokens) {
+        const int64_t nid = ids[nx];
+        if (nid >= 0 && nid < vocab) pending = b ^ 1;
+      }
+    }
+    const float mu = mean[tok], r = rstd[tok];
+    const float* xs = gbuf + b * 2 * dim;
+    const float* ds = xs + dim;
+    float s[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int k = 0; k < kSChunks; ++k) {
+      const int c = t + kSG * k;
+      if (c < nch) {
+        const float4 x = *reinterpret_cast<const float4*>(xs + 4 * c);
+        const float4 d = *reinterpret_cast<const float4*>(ds + 4 * c);
+        const float4 g = ldg4(gamma + 4 * c);
+        const float4 xh = make_float4(__fmul_rn(__fsub_rn(x.x, mu), r), __fmul_rn(__fsub_rn(x.y, mu), r),
+                                      __fmul_rn(__fsub_rn(x.z, mu), r), __fmul_rn(__fsub_rn(x.w, mu), r));
+        const float4 gg = make_float4(__fmul_rn(d.x, g.x), __fmul_rn(d.y, g.y), __fmul_rn(d.z, g.z), __fmul_rn(d.w, g.w));
+        s[0] = __fadd_rn(s[0], __fadd_rn(__fadd_rn(gg.x, gg.y), __fadd_rn(gg.z, gg.w)));
+        s[1] = __fadd_rn(s[1], __fadd_rn(__fadd_rn(__fmul_rn(gg.x, xh.x), __fmul_rn(gg.y, xh.y)),
+                                         __fadd_rn(__fmul_rn(gg.z, xh.z), __fmul_rn(gg.w, xh.w))));
+        if (ok) {
+          pg[k].x = __fadd_rn(pg[k].x, __fmul_rn(d.x, xh.x));
+          pg[k].y = __fadd_rn(pg[k].y, __fmul_rn(d.y, xh.y));
+          pg[k].z = __fadd_rn(pg[k].z, __fmul_rn(d.z, xh.z));
+          pg[k].w = __fadd_rn(pg[k].w, __fmul_rn(d.w, xh.w));
+          pb[k].x = __fadd_rn(pb[k].x, d.x);
+          pb[k].y = __fadd_rn(pb[k].y, d.y);
+          pb[k].z = __fadd_rn(pb[k].z, d.z);
+          pb[k].w = __fadd_rn(pb[k].w, d.w);
+        }
+      }
+    }
+    group_sum256<2>(s, s_red[group], slot, group, t);
+    slot ^= 1;
+    const float m1 = __fdiv_rn(s[0], fdim), m2 = __fdiv_rn(s[1], fdim);
+    float* dwrow = dw + id * static_cast<int64_t>(dim);
+#pragma unroll
+    for (int k = 0; k < kSChunks; ++k) {
+      const int c = t + kSG * k;
+      if (c < nch && ok) {
+        const float4 x = *reinterpret_cast<const float4*>(xs + 4 * c);
+        const float4 d = *reinterpret_cast<const float4*>(ds + 4 * c);
+        const float4 g = ldg4(gamma + 4 * c);
+        float4 dx;
+        dx.x = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d.x, g.x), m1), __fmul_rn(__fmul_rn(__fsub_rn(x.x, mu), r), m2)));
+        dx.y = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d.y, g.y), m1), __fmul_rn(__fmul_rn(__fsub_rn(x.y, mu), r), m2)));
+        dx.z = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d.z, g.z), m1), __fmul_rn(__fmul_rn(__fsub_rn(x.z, mu), r), m2)));
+        dx.w = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d.w, g.w), m1), __fmul_rn(__fmul_rn(__fsub_rn(x.w, mu), r), m2)));
+        red_add4(dwrow + 4 * c, dx);
+      }
+    }
+  }
+  // a group that gave up lets its copy in flight land (bounded) before the
+  // buffers are reused below
+  if (t == 0 && pending >= 0 && s_abort[group]) mbar_wait(&s_full[group][pending], (phase >> pending) & 1u);
+  __syncthreads();
+  // partials: each group's into its first buffer, then summed over the groups in order
+  float* const part = s_buf + static_cast<int64_t>(group) * 4 * dim;
+#pragma unroll
+  for (int k = 0; k < kSChunks; ++k) {
+    const int c = t + kSG * k;
+    if (c < nch) {
+      *reinterpret_cast<float4*>(part + 4 * c) = pg[k];
+      *reinterpret_cast<float4*>(part + dim + 4 * c) = pb[k];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < dim; i += blockDim.x) {
+    float a = 0.0f, bsum = 0.0f;
+#pragma unroll
+    for (int gi = 0; gi < kSGroups; ++gi) {
+      a = __fadd_rn(a, s_buf[static_cast<int64_t>(gi) * 4 * dim + i]);
+      bsum = __fadd_rn(bsum, s_buf[static_cast<int64_t>(gi) * 4 * dim + dim + i]);
+    }
+    atomicAdd(dgamma + i, a);
+    atomicAdd(dbeta + i, bsum);
+  }
+}
+
+// --------------------------------------------------------------------------
 // host side
 
 struct EmbedDevice {
@@ -403,8 +528,8 @@ bwd_status ensure_device(EmbedDevice** out) {
   if (!d.ready) {
     if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute");
-    if ((e = cudaFuncSetAttribute(reinterpret_cast<const void*>(embed_bwd_kernel),
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bwd_smem_bytes(kFastMaxDim))) !=
+    if ((e = cudaFuncSetAttribute(reinterpret_cast<const void*>(embed_bwd_staged_kernel),
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, staged_smem_bytes(kFastMaxDim))) !=
         cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
     struct { const void* fn; int threads; int* out; } occ[] = {
@@ -462,6 +587,21 @@ bwd_status bwd_embedding_init(const uint32_t* words, int64_t num_embeddings, int
   return check_launch("embed_init_kernel launch");
 }
 
+bwd_status bwd_check_device(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int fault = 0;
+  if ((e = cudaMemcpyFromSymbol(&fault, g_embed_fault, sizeof fault)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemcpyFromSymbol(fault word)");
+  if (fault == 0) return BWD_OK;
+  const unsigned int zero = 0;
+  if ((e = cudaMemcpyToSymbol(g_embed_fault, &zero, sizeof zero)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemcpyToSymbol(fault word)");
+  return fail(BWD_ERR_CUDA, "a bounded wait for a bulk copy in a library kernel gave up; the outputs of the "
+                            "kernels since the last check are unspecified");
+}
+
 float bwd_embedding_xavier_bound(int64_t num_embeddings, int64_t dim) {
   if (num_embeddings < 1 || dim < 1) return -1.0f;
   return static_cast<float>(std::sqrt(6.0 / (static_cast<double>(num_embeddings) + static_cast<double>(dim))));
@@ -516,15 +656,10 @@ bwd_status bwd_embedding_backward(const int64_t* ids, int64_t num_tokens, const 
   const bool fast = dim % 4 == 0 && dim <= kFastMaxDim && aligned16(weight) && aligned16(gamma) &&
                     aligned16(dy) && aligned16(dweight);
   if (fast) {
-    const int smem = bwd_smem_bytes(static_cast<int>(dim));
-    int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, reinterpret_cast<const void*>(embed_bwd_kernel), kGroup * kBwdGroups, smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-    embed_bwd_kernel<<<grid_for(num_tokens, kBwdGroups, d->num_sms, occ > 0 ? occ : 1), kGroup * kBwdGroups, smem,
-                       st>>>(ids, num_tokens, weight, num_embeddings, static_cast<int>(dim), gamma, mean, rstd, dy,
-                             dweight, dgamma, dbeta);
-    return check_launch("embed_bwd_kernel launch");
+    embed_bwd_staged_kernel<<<grid_for(num_tokens, kSGroups, d->num_sms, 1), kSG * kSGroups,
+                              staged_smem_bytes(static_cast<int>(dim)), st>>>(
+        ids, num_tokens, weight, num_embeddings, static_cast<int>(dim), gamma, mean, rstd, dy, dweight, dgamma, dbeta);
+    return check_launch("embed_bwd_staged_kernel launch");
   }
   embed_bwd_slow_kernel<<<grid_for(num_tokens, kSlowGroups, d->num_sms, d->occ_slow_bwd), kGroup * kSlowGroups, 0,
                           st>>>(ids, num_tokens, weight, num_embeddings, dim, gamma, mean, rstd, dy, dweight, dgamma,

@@ -223,6 +223,14 @@ bwd_status bwd_embedding_backward(const int64_t* ids, int64_t num_tokens,
                                   const float* dy, float* dweight,
                                   float* dgamma, float* dbeta, void* stream);
 
+/* Waits for `stream` and reports whether a bounded wait inside one of the
+ * library's kernels gave up since the last check (the staged embedding
+ * backward waits for its own bulk copies; each wait gives up after about a
+ * second, flags the device and lets the kernel return).  BWD_OK, or
+ * BWD_ERR_CUDA with bwd_last_error() describing it; the flag is cleared.
+ * Blocking; not callable during stream capture. */
+bwd_status bwd_check_device(void* stream);
+
 /* Static description of a status code. */
 const char* bwd_status_string(bwd_status status);
 

@@ -309,3 +309,19 @@ def test_full_size_embed_7b_sampled(E):
     for got, ref, s in ((dg, rg, sg), (db, rb, sb)):
         tol = 2 * (128 + t) * U * s
         assert np.all(np.abs(got.cpu().numpy() - ref) <= tol)
+
+
+def test_device_check_after_staged_backward(E):
+    """The staged backward's bounded waits complete in normal operation: the
+    device fault flag stays clear."""
+    import block_wise_dynamic_gb300 as bwd
+
+    d, v = 4096, 500
+    w = torch.from_numpy(rand_weight(v, d, 70)).to(dev())
+    g, b = (torch.from_numpy(a).to(dev()) for a in affine(d, 71))
+    ids = torch.from_numpy(ids_for(5000, v, 72)).to(dev())
+    _, mean, rstd = E.forward(ids, w, g, b)
+    dy = torch.randn(5000, d, device=dev())
+    for _ in range(3):
+        E.backward(ids, w, g, mean, rstd, dy, torch.zeros_like(w), torch.zeros_like(g), torch.zeros_like(g))
+    bwd.check_device(0)
