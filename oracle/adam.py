@@ -26,9 +26,10 @@ Readings where the page is silent:
   t counts from 1; the state before step 1 is all codes of +0.0 with absmax 0
   (R6), which dequantizes to exact zeros.  bf16 gradients widen exactly.
 
-bf16 parameters (the page's low-precision weights with a high-precision
-update): p is widened to binary32, updated as above, and rounded back to bf16
-(nearest, ties to even).
+bf16 or fp16 parameters (the page's low-precision weights with a
+high-precision update; the page itself names FP16): p is widened to binary32,
+updated as above, and rounded back to bf16 / IEEE binary16 (nearest, ties to
+even).  fp16 gradients widen exactly, like bf16 ones.
 
 Decoupled weight decay (AdamW; not on the page, the first extension of the
 method): with weight_decay wd > 0 the parameters are first scaled,
@@ -106,6 +107,19 @@ def round_to_bf16(x) -> np.ndarray:
     return r.astype(np.uint16)
 
 
+def widen_f16(bits) -> np.ndarray:
+    """IEEE binary16 bit patterns (uint16) to binary32 (exact)."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def round_to_f16(x) -> np.ndarray:
+    """binary32 -> IEEE binary16 bit patterns, round to nearest, ties to
+    even, with gradual underflow and overflow to infinity (NumPy's
+    conversion, used here as a library step)."""
+    with np.errstate(over="ignore"):  # overflow to infinity is the rounding rule
+        return np.asarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
 def adam_update_fp32(p, g, m_old, v_old, hp: AdamHParams):
     """One binary32 Adam(W) update (R10).  Returns new (p, m, v); inputs unchanged."""
     if hp.weight_decay < 0.0:
@@ -123,18 +137,25 @@ def adam_update_fp32(p, g, m_old, v_old, hp: AdamHParams):
     return p_new.astype(F32), m.astype(F32), v.astype(F32)
 
 
-def adam8bit_step(p, g, m_codes, m_absmax, v_codes, v_absmax, hp: AdamHParams, p_bf16: bool = False):
+def adam8bit_step(p, g, m_codes, m_absmax, v_codes, v_absmax, hp: AdamHParams, p_bf16: bool = False,
+                  p_f16: bool = False):
     """One 8-bit Adam step on one flat tensor (R9-R11).
 
     Returns new ``(p, m_codes, m_absmax, v_codes, v_absmax)``.  With
-    ``p_bf16`` the parameters are bf16 bit patterns (uint16): they are
-    widened to binary32 for the update and rounded back to bf16.
+    ``p_bf16`` (``p_f16``) the parameters are bf16 (IEEE binary16) bit
+    patterns (uint16): they are widened to binary32 for the update and
+    rounded back to nearest, ties to even.
     """
     m_old = dequantize_blockwise(m_codes, m_absmax, signed=True)
     v_old = dequantize_blockwise(v_codes, v_absmax, signed=False)
+    if p_bf16 and p_f16:
+        raise ValueError("p_bf16 and p_f16 exclude each other")
     if p_bf16:
         p32, m, v = adam_update_fp32(widen_bf16(p), g, m_old, v_old, hp)
         p_new = round_to_bf16(p32)
+    elif p_f16:
+        p32, m, v = adam_update_fp32(widen_f16(p), g, m_old, v_old, hp)
+        p_new = round_to_f16(p32)
     else:
         p_new, m, v = adam_update_fp32(p, g, m_old, v_old, hp)
     mc, ma = quantize_blockwise(m, signed=True)

@@ -225,3 +225,53 @@ def test_8bit_step_with_bf16_params_rounds_the_fp32_update():
     assert np.array_equal(out[0], round_to_bf16(ref32[0]))
     for a, b in zip(out[1:], ref32[1:]):
         assert np.array_equal(a, b)
+
+
+def test_widen_f16_matches_torch_for_every_pattern():
+    from oracle.adam import widen_f16
+
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = widen_f16(bits)
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.float16).float().numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+
+
+def test_round_to_f16_matches_torch_conversion():
+    """round_to_f16 against torch's float32 -> float16 conversion: random
+    values across the binary16 range, exact ties between neighbours, the
+    subnormal range, the overflow edge, signed zeros and NaN."""
+    from oracle.adam import round_to_f16
+
+    rng = np.random.default_rng(7)
+    vals = [rng.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(-8, 5, 20000).astype(np.float32)]
+    h = np.arange(0, 0x7C00, 37, dtype=np.uint32).astype(np.uint16)  # finite binary16 patterns
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    vals.append(((lo + hi) / 2).astype(np.float32))                   # exact ties (representable in binary32)
+    vals.append(np.array([65504.0, 65519.0, 65520.0, 65536.0, 1e-8, 6e-8, 5.96e-8, 2.98e-8, 0.0, -0.0,
+                          float("inf"), -float("inf")], np.float32))
+    arr = np.concatenate(vals).astype(np.float32)
+    got = round_to_f16(arr)
+    want = torch.from_numpy(arr).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+    assert np.isnan(round_to_f16(np.array([np.nan], np.float32)).view(np.float16)[0])
+
+
+def test_f16_parameter_step_is_the_fp32_step_rounded():
+    from oracle.adam import round_to_f16, widen_f16
+
+    rng = np.random.default_rng(8)
+    n = 3 * 2048 + 17
+    p = round_to_f16((rng.standard_normal(n) * 0.02).astype(np.float32))
+    g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    st = oracle.state_init(n)
+    hp = oracle.AdamHParams(lr=1e-3, step=1)
+    out = oracle.adam8bit_step(p, g, *st, hp, p_f16=True)
+    ref32 = oracle.adam8bit_step(widen_f16(p), g, *st, hp)
+    assert np.array_equal(out[0], round_to_f16(ref32[0]))
+    for a, b in zip(out[1:], ref32[1:]):
+        assert np.array_equal(a, b)
+    with pytest.raises(ValueError):
+        oracle.adam8bit_step(p, g, *st, hp, p_bf16=True, p_f16=True)
