@@ -52,7 +52,7 @@ def parse_args():
     ap.add_argument("--workload", default="llama2_7b",
                     choices=["llama2_7b", "gpt_350m", "ragged_2000", "adam_1m", "quant_2p28", "embed_7b"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--param-dtype", default="f32", choices=["f32", "bf16"],
+    ap.add_argument("--param-dtype", default="f32", choices=["f32", "bf16", "f16"],
                     help="parameter storage (bf16: widened for the update, rounded back)")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -360,8 +360,8 @@ def run_ours(args):
     sizes = [n for n in wl.sizes if n > 0]
     N = sum(sizes)
     gbytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
-    pdtype = torch.bfloat16 if args.param_dtype == "bf16" else torch.float32
-    pbytes = 2 if pdtype == torch.bfloat16 else 4
+    pdtype = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[args.param_dtype]
+    pbytes = 4 if pdtype == torch.float32 else 2
     bpp = algorithmic_bytes_per_param(gbytes, pbytes)
 
     ps, gs, sts = [], [], []

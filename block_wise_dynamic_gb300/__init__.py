@@ -38,7 +38,7 @@ __all__ = [
 ]
 
 _KINDS = {"signed": _abi.BWD_MAP_SIGNED, "unsigned": _abi.BWD_MAP_UNSIGNED}
-_GDT = {torch.float32: _abi.BWD_F32, torch.bfloat16: _abi.BWD_BF16}
+_GDT = {torch.float32: _abi.BWD_F32, torch.bfloat16: _abi.BWD_BF16, torch.float16: _abi.BWD_F16}
 
 
 class _Lib:
@@ -163,15 +163,15 @@ def _hparams(lr, beta1, beta2, eps, step, weight_decay=0.0) -> _abi.AdamHParams:
 def adam8bit_step(p, g, m_codes, m_absmax, v_codes, v_absmax, *, lr=1e-3, beta1=0.9, beta2=0.999,
                   eps=1e-8, weight_decay=0.0, step, stream=None) -> None:
     """One 8-bit Adam step on one flat tensor, in place (``bwd_adam8bit_step``);
-    ``weight_decay`` > 0 makes it AdamW (decoupled).  bf16 parameters go
-    through ``bwd_adam8bit_step_multi_ex``."""
-    if isinstance(p, torch.Tensor) and p.dtype == torch.bfloat16:
+    ``weight_decay`` > 0 makes it AdamW (decoupled).  bf16 and fp16
+    parameters go through ``bwd_adam8bit_step_multi_ex``."""
+    if isinstance(p, torch.Tensor) and p.dtype in (torch.bfloat16, torch.float16):
         return adam8bit_step_multi([p], [g], [m_codes], [m_absmax], [v_codes], [v_absmax], lr=lr, beta1=beta1,
                                    beta2=beta2, eps=eps, weight_decay=weight_decay, step=step, stream=stream)
     n = p.numel()
     _need(p, "p", torch.float32)
     if g.dtype not in _GDT:
-        raise TypeError("g must be float32 or bfloat16")
+        raise TypeError("g must be float32, bfloat16 or float16")
     _need(g, "g", g.dtype, n)
     _need(m_codes, "m_codes", torch.uint8, n)
     _need(v_codes, "v_codes", torch.uint8, n)
@@ -207,7 +207,7 @@ class MultiTensorArgs:
             n = params[i].numel()
             _need(params[i], f"params[{i}]", params[i].dtype)
             if params[i].dtype not in _GDT:
-                raise TypeError("parameters must be float32 or bfloat16")
+                raise TypeError("parameters must be float32, bfloat16 or float16")
             _need(grads[i], f"grads[{i}]", grads[i].dtype, n)
             _need(m_codes[i], f"m_codes[{i}]", torch.uint8, n)
             _need(v_codes[i], f"v_codes[{i}]", torch.uint8, n)

@@ -20,6 +20,7 @@ BWD_MAP_SIGNED = 0
 BWD_MAP_UNSIGNED = 1
 BWD_F32 = 0
 BWD_BF16 = 1
+BWD_F16 = 2
 BLOCK = 2048
 
 

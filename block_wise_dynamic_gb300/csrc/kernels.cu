@@ -31,6 +31,7 @@
 // the threshold compare.  The Adam update uses the same operations, in the
 // same order, as the CPU oracle.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -383,17 +384,32 @@ struct AdamArgs {
 
 static_assert(sizeof(AdamArgs) <= 32764, "kernel parameter space");
 
-template <bool kBf16>
-__device__ __forceinline__ void load_grad4(const void* g, int64_t e, float* out) {
-  if (kBf16) {
-    const uint2 a = ld_stream_u2(static_cast<const uint16_t*>(g) + e);
-    out[0] = __uint_as_float(a.x << 16);
-    out[1] = __uint_as_float(a.x & 0xffff0000u);
-    out[2] = __uint_as_float(a.y << 16);
-    out[3] = __uint_as_float(a.y & 0xffff0000u);
-  } else {
-    const float4 a = ld_stream_f4(static_cast<const float*>(g) + e);
+// Element types of parameters and gradients (the values of bwd_dtype).
+constexpr int kF32 = BWD_F32, kBF16 = BWD_BF16, kF16 = BWD_F16;
+
+template <int kT>
+__host__ __device__ constexpr uint32_t elem_bytes() { return kT == kF32 ? 4u : 2u; }
+
+// Four consecutive elements of type kT widened to fp32 (bf16 and fp16 widen
+// exactly).
+template <int kT>
+__device__ __forceinline__ void load4(const void* base, int64_t e, float* out) {
+  if (kT == kF32) {
+    const float4 a = ld_stream_f4(static_cast<const float*>(base) + e);
     out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+  } else {
+    const uint2 a = ld_stream_u2(static_cast<const uint16_t*>(base) + e);
+    if (kT == kBF16) {
+      out[0] = __uint_as_float(a.x << 16);
+      out[1] = __uint_as_float(a.x & 0xffff0000u);
+      out[2] = __uint_as_float(a.y << 16);
+      out[3] = __uint_as_float(a.y & 0xffff0000u);
+    } else {
+      out[0] = __half2float(__ushort_as_half(static_cast<unsigned short>(a.x & 0xffffu)));
+      out[1] = __half2float(__ushort_as_half(static_cast<unsigned short>(a.x >> 16)));
+      out[2] = __half2float(__ushort_as_half(static_cast<unsigned short>(a.y & 0xffffu)));
+      out[3] = __half2float(__ushort_as_half(static_cast<unsigned short>(a.y >> 16)));
+    }
   }
 }
 
@@ -411,21 +427,26 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return r;
 }
 
-// One fp32 or bf16 element, widened to fp32 (bf16 widening is exact).
-template <bool kBf16>
-__device__ __forceinline__ float load_grad1(const void* g, int64_t i) {
-  if (kBf16) return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(g)[i]) << 16);
-  return static_cast<const float*>(g)[i];
+// One element of type kT, widened to fp32.
+template <int kT>
+__device__ __forceinline__ float load1(const void* base, int64_t i) {
+  if (kT == kF32) return static_cast<const float*>(base)[i];
+  const unsigned short h = static_cast<const unsigned short*>(base)[i];
+  if (kT == kBF16) return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  return __half2float(__ushort_as_half(h));
 }
 
-// bf16 bits of x, round to nearest even (CUDA's conversion).
-__device__ __forceinline__ uint32_t bf16_bits(float x) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
+// 16-bit pattern of x as a bf16 or fp16 value, round to nearest even
+// (CUDA's conversions).
+template <int kT>
+__device__ __forceinline__ uint32_t bits16(float x) {
+  if (kT == kBF16) return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
+  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(x)));
 }
 
-// kBf16: gradient type; kPBf16: parameter type (bf16 parameters are widened
-// for the update and rounded back to bf16 on store).
-template <bool kBf16, bool kPBf16>
+// kG: gradient type; kP: parameter type (kF32, kBF16 or kF16; 16-bit
+// parameters are widened for the update and rounded back on store).
+template <int kG, int kP>
 __global__ void __launch_bounds__(kCta, 1)
 adam8bit_kernel(const __grid_constant__ AdamArgs args) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -474,8 +495,8 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
         const TensorArgs& N = args.t[tn];
         const int64_t bn = (gn - args.block_start[tn]) * BWD_BLOCK;
         if (N.vec && N.n - bn >= BWD_BLOCK) {
-          if (t == 0) prefetch_l2(static_cast<const char*>(N.p) + bn * (kPBf16 ? 2 : 4), kPBf16 ? 4096u : 8192u);
-          else if (t == 1) prefetch_l2(static_cast<const char*>(N.g) + bn * (kBf16 ? 2 : 4), kBf16 ? 4096u : 8192u);
+          if (t == 0) prefetch_l2(static_cast<const char*>(N.p) + bn * elem_bytes<kP>(), BWD_BLOCK * elem_bytes<kP>());
+          else if (t == 1) prefetch_l2(static_cast<const char*>(N.g) + bn * elem_bytes<kG>(), BWD_BLOCK * elem_bytes<kG>());
           else if (t == 2) prefetch_l2(N.mc + bn, 2048u);
           else prefetch_l2(N.vc + bn, 2048u);
         }
@@ -488,8 +509,8 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
 #pragma unroll
       for (int k = 0; k < kQuads; ++k) {
         const int64_t e = base + kSpan * k + 4 * t;
-        load_grad4<kPBf16>(T.p, e, &p[4 * k]);
-        load_grad4<kBf16>(T.g, e, &g[4 * k]);
+        load4<kP>(T.p, e, &p[4 * k]);
+        load4<kG>(T.g, e, &g[4 * k]);
         mw[k] = ld_stream_u1(T.mc + e);
         vw[k] = ld_stream_u1(T.vc + e);
       }
@@ -503,8 +524,8 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
         for (int j = 0; j < 4; ++j) {
           const int e = slot(t, 4 * k + j);
           const bool in = e < rem;
-          p[4 * k + j] = in ? load_grad1<kPBf16>(T.p, base + e) : 0.0f;
-          g[4 * k + j] = in ? load_grad1<kBf16>(T.g, base + e) : 0.0f;
+          p[4 * k + j] = in ? load1<kP>(T.p, base + e) : 0.0f;
+          g[4 * k + j] = in ? load1<kG>(T.g, base + e) : 0.0f;
           cm[j] = in ? T.mc[base + e] : 128u;
           cv[j] = in ? T.vc[base + e] : 0u;
         }
@@ -548,10 +569,10 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
 #pragma unroll
       for (int k = 0; k < kQuads; ++k) {
         const int64_t e = base + kSpan * k + 4 * t;
-        if (kPBf16)
+        if (kP != kF32)
           __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(T.p) + e),
-                 make_uint2(bf16_bits(p[4 * k]) | (bf16_bits(p[4 * k + 1]) << 16),
-                            bf16_bits(p[4 * k + 2]) | (bf16_bits(p[4 * k + 3]) << 16)));
+                 make_uint2(bits16<kP>(p[4 * k]) | (bits16<kP>(p[4 * k + 1]) << 16),
+                            bits16<kP>(p[4 * k + 2]) | (bits16<kP>(p[4 * k + 3]) << 16)));
         else
           __stcs(reinterpret_cast<float4*>(static_cast<float*>(T.p) + e),
                  make_float4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]));
@@ -561,7 +582,7 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
       for (int j = 0; j < kPer; ++j) {
         const int e = slot(t, j);
         if (e < rem) {
-          if (kPBf16) static_cast<uint16_t*>(T.p)[base + e] = static_cast<uint16_t>(bf16_bits(p[j]));
+          if (kP != kF32) static_cast<uint16_t*>(T.p)[base + e] = static_cast<uint16_t>(bits16<kP>(p[j]));
           else static_cast<float*>(T.p)[base + e] = p[j];
         }
       }
@@ -643,7 +664,7 @@ struct DeviceState {
   int num_sms = 0;
   int occ_quant[2] = {0, 0};
   int occ_dequant[2] = {0, 0};
-  int occ_adam[4] = {0, 0, 0, 0};  // [2 * parameter bf16 + gradient bf16]
+  int occ_adam[9] = {};  // [3 * parameter type + gradient type]
 };
 
 std::mutex g_mu;
@@ -690,15 +711,17 @@ bwd_status ensure_device(DeviceState** out) {
                        reinterpret_cast<const void*>(quantize_kernel<false>)};
   const void* kd[2] = {reinterpret_cast<const void*>(dequantize_kernel<true>),
                        reinterpret_cast<const void*>(dequantize_kernel<false>)};
-  const void* ka[4] = {reinterpret_cast<const void*>(adam8bit_kernel<false, false>),
-                       reinterpret_cast<const void*>(adam8bit_kernel<true, false>),
-                       reinterpret_cast<const void*>(adam8bit_kernel<false, true>),
-                       reinterpret_cast<const void*>(adam8bit_kernel<true, true>)};
+  const void* ka[9] = {
+      reinterpret_cast<const void*>(adam8bit_kernel<kF32, kF32>), reinterpret_cast<const void*>(adam8bit_kernel<kBF16, kF32>),
+      reinterpret_cast<const void*>(adam8bit_kernel<kF16, kF32>), reinterpret_cast<const void*>(adam8bit_kernel<kF32, kBF16>),
+      reinterpret_cast<const void*>(adam8bit_kernel<kBF16, kBF16>), reinterpret_cast<const void*>(adam8bit_kernel<kF16, kBF16>),
+      reinterpret_cast<const void*>(adam8bit_kernel<kF32, kF16>), reinterpret_cast<const void*>(adam8bit_kernel<kBF16, kF16>),
+      reinterpret_cast<const void*>(adam8bit_kernel<kF16, kF16>)};
   for (int k = 0; k < 2; ++k) {
     if ((s = occupancy(kq[k], kQCta, kTablesBytes, &d.occ_quant[k])) != BWD_OK) return s;
     if ((s = occupancy(kd[k], kDeqThreads, 0, &d.occ_dequant[k])) != BWD_OK) return s;
   }
-  for (int k = 0; k < 4; ++k)
+  for (int k = 0; k < 9; ++k)
     if ((s = occupancy(ka[k], kCta, kTablesBytes, &d.occ_adam[k])) != BWD_OK) return s;
   d.ready = true;
   *out = &d;
@@ -744,17 +767,25 @@ void fill_scalars(const bwd_adam_hparams* hp, AdamArgs* a) {
   a->decay = static_cast<float>(1.0 - static_cast<double>(hp->lr) * static_cast<double>(hp->weight_decay));
 }
 
-bwd_status launch_adam_chunk(const AdamArgs& a, bool g_bf16, bool p_bf16, const DeviceState& d,
-                             cudaStream_t st) {
+template <int kG, int kP>
+void launch_typed(const AdamArgs& a, int grid, cudaStream_t st) {
+  adam8bit_kernel<kG, kP><<<grid, kCta, kTablesBytes, st>>>(a);
+}
+
+bwd_status launch_adam_chunk(const AdamArgs& a, int g_type, int p_type, const DeviceState& d, cudaStream_t st) {
   const int64_t total = a.block_start[a.num_tensors];
   if (total == 0) return BWD_OK;
-  const int grid = grid_for(total, kGroups, d, d.occ_adam[2 * p_bf16 + g_bf16]);
-  if (p_bf16) {
-    if (g_bf16) adam8bit_kernel<true, true><<<grid, kCta, kTablesBytes, st>>>(a);
-    else adam8bit_kernel<false, true><<<grid, kCta, kTablesBytes, st>>>(a);
-  } else {
-    if (g_bf16) adam8bit_kernel<true, false><<<grid, kCta, kTablesBytes, st>>>(a);
-    else adam8bit_kernel<false, false><<<grid, kCta, kTablesBytes, st>>>(a);
+  const int grid = grid_for(total, kGroups, d, d.occ_adam[3 * p_type + g_type]);
+  switch (3 * p_type + g_type) {
+    case 0: launch_typed<kF32, kF32>(a, grid, st); break;
+    case 1: launch_typed<kBF16, kF32>(a, grid, st); break;
+    case 2: launch_typed<kF16, kF32>(a, grid, st); break;
+    case 3: launch_typed<kF32, kBF16>(a, grid, st); break;
+    case 4: launch_typed<kBF16, kBF16>(a, grid, st); break;
+    case 5: launch_typed<kF16, kBF16>(a, grid, st); break;
+    case 6: launch_typed<kF32, kF16>(a, grid, st); break;
+    case 7: launch_typed<kBF16, kF16>(a, grid, st); break;
+    default: launch_typed<kF16, kF16>(a, grid, st); break;
   }
   return check_launch("adam8bit_kernel launch");
 }
@@ -855,9 +886,9 @@ bwd_status step_multi(int32_t num_tensors, PP p, bwd_dtype p_dtype, const void* 
                       uint8_t* const* m_codes, float* const* m_absmax, uint8_t* const* v_codes,
                       float* const* v_absmax, const int64_t* n, const bwd_adam_hparams* hp, void* stream) {
   if (num_tensors < 0) return fail(BWD_ERR_INVALID_ARG, "num_tensors < 0");
-  if (g_dtype != BWD_F32 && g_dtype != BWD_BF16)
+  if (g_dtype != BWD_F32 && g_dtype != BWD_BF16 && g_dtype != BWD_F16)
     return fail(BWD_ERR_UNSUPPORTED_DTYPE, "gradient dtype %d", (int)g_dtype);
-  if (p_dtype != BWD_F32 && p_dtype != BWD_BF16)
+  if (p_dtype != BWD_F32 && p_dtype != BWD_BF16 && p_dtype != BWD_F16)
     return fail(BWD_ERR_UNSUPPORTED_DTYPE, "parameter dtype %d", (int)p_dtype);
   bwd_status s = check_hparams(hp);
   if (s != BWD_OK) return s;
@@ -869,7 +900,7 @@ bwd_status step_multi(int32_t num_tensors, PP p, bwd_dtype p_dtype, const void* 
     if (n[i] < 0) return fail(BWD_ERR_INVALID_ARG, "tensor %d: n < 0", i);
     if (n[i] > 0 && (!p[i] || !g[i] || !m_codes[i] || !m_absmax[i] || !v_codes[i] || !v_absmax[i]))
       return fail(BWD_ERR_INVALID_ARG, "tensor %d: NULL pointer", i);
-    if (n[i] > 0 && (!aligned_to(p[i], p_dtype == BWD_BF16 ? 2 : 4) || !aligned_to(g[i], g_dtype == BWD_BF16 ? 2 : 4) ||
+    if (n[i] > 0 && (!aligned_to(p[i], p_dtype == BWD_F32 ? 4 : 2) || !aligned_to(g[i], g_dtype == BWD_F32 ? 4 : 2) ||
                      !aligned_to(m_absmax[i], 4) || !aligned_to(v_absmax[i], 4)))
       return fail(BWD_ERR_INVALID_ARG, "tensor %d: pointer not aligned to its element size", i);
     any_work = any_work || n[i] > 0;
@@ -880,7 +911,7 @@ bwd_status step_multi(int32_t num_tensors, PP p, bwd_dtype p_dtype, const void* 
 
   static thread_local AdamArgs a;  // ~32 KB: kept off the stack
   fill_scalars(hp, &a);
-  const bool g_bf16 = g_dtype == BWD_BF16, p_bf16 = p_dtype == BWD_BF16;
+  const int g_type = static_cast<int>(g_dtype), p_type = static_cast<int>(p_dtype);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int k = 0;
   a.block_start[0] = 0;
@@ -899,14 +930,14 @@ bwd_status step_multi(int32_t num_tensors, PP p, bwd_dtype p_dtype, const void* 
     ++k;
     if (k == kMaxTensors) {
       a.num_tensors = k;
-      if ((s = launch_adam_chunk(a, g_bf16, p_bf16, *d, st)) != BWD_OK) return s;
+      if ((s = launch_adam_chunk(a, g_type, p_type, *d, st)) != BWD_OK) return s;
       k = 0;
       a.block_start[0] = 0;
     }
   }
   if (k > 0) {
     a.num_tensors = k;
-    if ((s = launch_adam_chunk(a, g_bf16, p_bf16, *d, st)) != BWD_OK) return s;
+    if ((s = launch_adam_chunk(a, g_type, p_type, *d, st)) != BWD_OK) return s;
   }
   return BWD_OK;
 }

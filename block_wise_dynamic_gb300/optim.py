@@ -9,8 +9,9 @@ class is that switch:
 
 ``AdamW8bit`` is the same with decoupled weight decay.
 
-Parameters are fp32 (master weights) or bf16 CUDA tensors (widened for the
-update, stored back rounded to nearest even); gradients fp32 or bf16.  Per parameter the state holds ``step`` and the codes and absmax of
+Parameters are fp32 (master weights), bf16 or fp16 CUDA tensors (widened for
+the update, stored back rounded to nearest even); gradients fp32, bf16 or
+fp16.  Per parameter the state holds ``step`` and the codes and absmax of
 both moments; ``state_dict()`` / ``load_state_dict()`` round-trip them
 exactly.  Each ``step()`` issues one multi-tensor launch per (device,
 gradient dtype, step count) group.
@@ -62,8 +63,8 @@ class Adam8bit(torch.optim.Optimizer):
             for p in group["params"]:
                 if p.grad is None:
                     continue
-                if p.dtype not in (torch.float32, torch.bfloat16) or not p.is_cuda:
-                    raise TypeError("Adam8bit needs fp32 or bf16 CUDA parameters")
+                if p.dtype not in (torch.float32, torch.bfloat16, torch.float16) or not p.is_cuda:
+                    raise TypeError("Adam8bit needs fp32, bf16 or fp16 CUDA parameters")
                 if p.grad.is_sparse:
                     raise TypeError("sparse gradients are not supported")
                 st = self._state_for(p)

@@ -59,8 +59,10 @@ typedef enum {
   BWD_MAP_UNSIGNED = 1  /* the sign bit reused as fraction (second moment)  */
 } bwd_map_kind;
 
-/* Gradient element types. */
-typedef enum { BWD_F32 = 0, BWD_BF16 = 1 } bwd_dtype;
+/* Element types of gradients and (for bwd_adam8bit_step_multi_ex) of
+ * parameters: fp32, bf16, IEEE binary16.  16-bit values widen exactly; 16-bit
+ * parameters are rounded back to nearest, ties to even. */
+typedef enum { BWD_F32 = 0, BWD_BF16 = 1, BWD_F16 = 2 } bwd_dtype;
 
 /* Adam hyper-parameters (section 一: first and second moment).  `step` is
  * the 1-based index t of the step being taken (bias corrections use it).
@@ -129,7 +131,8 @@ bwd_status bwd_state_init(uint8_t* m_codes, float* m_absmax, uint8_t* v_codes,
  * exactly those of IEEE arithmetic; the parameter update uses approximate
  * (rsqrt / rcp) arithmetic and is within a few ulps of the update term.
  *   p                : device float[n], updated in place.
- *   g                : device, float[n] or bf16[n] per g_dtype, read only.
+ *   g                : device, float[n], bf16[n] or fp16[n] per g_dtype, read
+ *                      only.
  *   m_codes, v_codes : device uint8[n], updated in place.
  *   m_absmax,v_absmax: device float[ceil(n/2048)], updated in place.
  *   hp               : host pointer; hp->step >= 1, lr and eps finite,
@@ -153,12 +156,13 @@ bwd_status bwd_adam8bit_step_multi(int32_t num_tensors, float* const* p,
                                    const bwd_adam_hparams* hp, void* stream);
 
 /* The multi-tensor step with the parameter type given: p_dtype BWD_F32
- * (as bwd_adam8bit_step_multi) or BWD_BF16.  bf16 parameters are widened to
- * fp32 for the update and stored back rounded to nearest even (the page's
- * low-precision state with a high-precision update, section 二, opening
- * paragraph); codes and absmax are the same as with fp32 parameters.
- *   p : HOST array of num_tensors device pointers to fp32[n] or bf16[n]
- *       parameters, updated in place.  Other arguments as above. */
+ * (as bwd_adam8bit_step_multi), BWD_BF16 or BWD_F16.  16-bit parameters are
+ * widened to fp32 for the update and stored back rounded to nearest even
+ * (the page's low-precision state with a high-precision update, section 二,
+ * opening paragraph, which names FP16); codes and absmax are the same as
+ * with fp32 parameters.
+ *   p : HOST array of num_tensors device pointers to fp32[n], bf16[n] or
+ *       fp16[n] parameters, updated in place.  Other arguments as above. */
 bwd_status bwd_adam8bit_step_multi_ex(int32_t num_tensors, void* const* p,
                                       bwd_dtype p_dtype, const void* const* g,
                                       bwd_dtype g_dtype, uint8_t* const* m_codes,

@@ -83,7 +83,7 @@ def run_gpu(bwd, p, g, st, hp: oracle.AdamHParams):
     return tuple(t.cpu().numpy() for t in (tp, tmc, tma, tvc, tva))
 
 
-@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("n", [1, 2047, 2048, 2049, 5 * B + 77, 1 << 20])
 def test_single_step_from_identical_state(bwd, n, gdt):
     p = W.gen_normal(n, 0.02, seed=n).numpy()
@@ -161,7 +161,7 @@ def _multi_case(bwd, sizes, gdt, seed, offsets=None):
         compare_step(got, ref)
 
 
-@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16, torch.float16])
 def test_multi_ragged_list(bwd, gdt):
     rng = np.random.default_rng(5)
     sizes = [int(s) for s in rng.integers(1, 40_000, 60)] + [0, 2048, 4096, 1, 0, 2049]
@@ -341,8 +341,8 @@ def test_step_on_tensor_larger_than_2p31_elements(bwd):
 
 
 def compare_bf16_params(p_bits, ref_bits):
-    """bf16 parameters: at most 1e-3 of them one bf16 unit apart (the fp32
-    update is within a few ulps, so it can land on the other side of a bf16
+    """bf16 (or fp16) parameters: at most 1e-3 of them one unit apart (the
+    fp32 update is within a few ulps, so it can land on the other side of a
     rounding boundary), none further."""
     a = p_bits.astype(np.int32)
     b = ref_bits.astype(np.int32)
@@ -397,3 +397,47 @@ def test_bf16_param_optimizer_and_single_tensor_call(bwd):
     mc, ma, vc, va = bwd.state_init(q.numel(), DEV)
     bwd.adam8bit_step(q, p.grad.view(-1), mc, ma, vc, va, lr=1e-3, step=1)
     assert q.dtype == torch.bfloat16
+
+
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16, torch.float16])
+def test_f16_params_step_from_identical_state(bwd, gdt):
+    """IEEE binary16 parameters (the page's FP16 state): widened for the
+    update, rounded back to nearest even; codes and absmax exact."""
+    from oracle.adam import round_to_f16
+
+    rng = np.random.default_rng(33)
+    sizes = [3 * B + 7, 2048, 5000]
+    ps = [torch.from_numpy(round_to_f16((rng.standard_normal(n) * 0.02).astype(np.float32)).view(np.int16))
+          .view(torch.float16) for n in sizes]
+    gs = [W.gen_normal(n, 1e-2, 60 + i, dtype=gdt) for i, n in enumerate(sizes)]
+    sts = [random_state(n, 70 + i) for i, n in enumerate(sizes)]
+    dp = [p.to(DEV) for p in ps]
+    dst = [to_dev(*st) for st in sts]
+    hp = oracle.AdamHParams(lr=1e-3, weight_decay=0.01, step=4)
+    bwd.adam8bit_step_multi(dp, [g.to(DEV) for g in gs], *[[s[k] for s in dst] for k in range(4)],
+                            lr=hp.lr, weight_decay=hp.weight_decay, step=hp.step)
+    torch.cuda.synchronize()
+    for i in range(len(sizes)):
+        pb = ps[i].view(torch.int16).numpy().view(np.uint16)
+        ref = oracle.adam8bit_step(pb, g_to_np(gs[i]), *sts[i], hp, p_f16=True)
+        compare_bf16_params(dp[i].cpu().view(torch.int16).numpy().view(np.uint16), ref[0])
+        for a, b in zip((x.cpu().numpy() for x in dst[i]), ref[1:]):
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def test_f16_param_optimizer(bwd):
+    from oracle.adam import widen_f16
+
+    torch.manual_seed(6)
+    p = torch.nn.Parameter((torch.randn(7000, device=DEV) * 0.02).to(torch.float16))
+    opt = bwd.Adam8bit([p], lr=1e-3)
+    ref = (p.detach().cpu().view(torch.int16).numpy().view(np.uint16).copy(), *oracle.state_init(7000))
+    for t in range(1, 4):
+        g = (torch.randn(7000, device=DEV) * 1e-2).to(torch.float16)
+        p.grad = g
+        opt.step()
+        ref = oracle.adam8bit_step(ref[0], widen_f16(g.cpu().view(torch.int16).numpy().view(np.uint16)), *ref[1:],
+                                   oracle.AdamHParams(lr=1e-3, step=t), p_f16=True)
+    st = opt.state[p]
+    compare_bf16_params(p.detach().cpu().view(torch.int16).numpy().view(np.uint16), ref[0])
+    assert np.array_equal(st["m_codes"].cpu().numpy(), ref[1]) and np.array_equal(st["v_codes"].cpu().numpy(), ref[3])
