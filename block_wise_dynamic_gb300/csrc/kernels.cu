@@ -28,8 +28,10 @@
 // absmax, the quotient x / absmax (exact_div.cuh gives the correctly rounded
 // quotient from a per-block reciprocal; tiny negative quotients, where -0.0
 // and a negative subnormal give different codes, fall back to div.rn) and
-// the threshold compare.  The Adam update uses the same operations, in the
-// same order, as the CPU oracle.
+// the threshold compare (an integer compare of pattern bits inside a bucket,
+// the same decision for every binary32 value; tables.h).  The moments use
+// the same operations, in the same order, as the CPU oracle; the parameter
+// update uses approximate rsqrt / rcp (a few ulps of the update term).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>

@@ -13,7 +13,8 @@
  * Conventions shared by every entry point
  *   - Pointers named "device" are CUDA device (or managed) memory of the
  *     CURRENT device; the caller owns them.  The library keeps only its own
- *     immutable code tables (about 32 KB per device, uploaded on first use).
+ *     immutable code tables (about 26 KB per device, uploaded on first use)
+ *     and one fault word (see bwd_check_device).
  *   - Every device operation is enqueued on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) and returns without waiting for it.  Launch
  *     errors are reported as BWD_ERR_CUDA; faults inside a kernel surface on
