@@ -153,19 +153,31 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_sha(path: str) -> str:
+    """sha256[:16] of a source file's code: comments and blank lines stripped,
+    so the committed ncu numbers stay tied to the code, not its comments."""
+    import re
+
+    src = open(path, encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    lines = [ln.strip() for ln in src.splitlines() if ln.strip()]
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def traffic_per_param():
     """DRAM bytes per parameter of the fused kernel from the committed ncu
     summary, valid only while the kernel source is the one profiled."""
     src = os.path.join(ROOT, "block_wise_dynamic_gb300", "csrc", "kernels.cu")
     prof = os.path.join(ROOT, "profiles", "adam8bit_kernel_llama2_7b.md")
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = code_sha(src)
         kv = {}
         for line in open(prof):
-            if ":" in line and line.startswith("- "):
-                k, v = line[2:].split(":", 1)
+            if ": " in line and line.startswith("- "):
+                k, v = line[2:].split(": ", 1)
                 kv[k.strip()] = v.strip().strip("`")
-        if kv.get("kernels.cu sha256[:16]") != sha:
+        if kv.get("kernels.cu code sha256[:16]") != sha:
             return None
         return float(kv["dram bytes per param"])
     except (OSError, KeyError, ValueError):
@@ -655,7 +667,7 @@ def embed_traffic():
     src = os.path.join(ROOT, "block_wise_dynamic_gb300", "csrc", "embedding.cu")
     prof = os.path.join(ROOT, "profiles", "embed_kernels_embed_7b.md")
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = code_sha(src)
         text = open(prof).read()
     except OSError:
         return None
