@@ -325,3 +325,34 @@ def test_device_check_after_staged_backward(E):
     for _ in range(3):
         E.backward(ids, w, g, mean, rstd, dy, torch.zeros_like(w), torch.zeros_like(g), torch.zeros_like(g))
     bwd.check_device(0)
+
+
+def test_backward_with_many_interleaved_invalid_ids(E):
+    """About 30% of 5,000 token ids out of range, spread through the list:
+    the staged backward issues no copy and takes no wait for them, so its
+    per-buffer phase bookkeeping is exercised across skipped tokens."""
+    d, v = 1024, 300
+    w = rand_weight(v, d, 80)
+    gamma, beta = affine(d, 81)
+    rng = np.random.default_rng(82)
+    ids = ids_for(5000, v, 83).copy()
+    bad = rng.random(ids.size) < 0.3
+    ids[bad] = np.where(rng.random(int(bad.sum())) < 0.5, -1 - rng.integers(0, 5, int(bad.sum())), v + rng.integers(0, 9, int(bad.sum())))
+    dy = rng.standard_normal((ids.size, d)).astype(np.float32)
+    ids_d = torch.from_numpy(ids).to(dev())
+    wd = torch.from_numpy(w).to(dev())
+    gd, bd = torch.from_numpy(gamma).to(dev()), torch.from_numpy(beta).to(dev())
+    y, mean, rstd = E.forward(ids_d, wd, gd, bd)
+    assert bool(torch.isnan(y[torch.from_numpy(bad).to(dev())]).all())
+    dw, dg, db = torch.zeros_like(wd), torch.zeros_like(gd), torch.zeros_like(gd)
+    E.backward(ids_d, wd, gd, mean, rstd, torch.from_numpy(dy).to(dev()), dw, dg, db)
+    torch.cuda.synchronize()
+    ok = ~bad
+    dy64 = dy[ok].astype(np.float64)
+    rw, rg, rb = se.backward(ids[ok], w, gamma, dy64)
+    sw, sg, sb = se.backward_abs_sums(ids[ok], w, gamma, dy64)
+    k = np.bincount(ids[ok], minlength=v)[:, None]
+    assert np.all(np.abs(dw.cpu().numpy() - rw) <= 2 * (128 + k) * U * sw + 1e-30)
+    t = int(ok.sum())
+    for got, ref, s in ((dg, rg, sg), (db, rb, sb)):
+        assert np.all(np.abs(got.cpu().numpy() - ref) <= 2 * (128 + t) * U * s + 1e-30)
