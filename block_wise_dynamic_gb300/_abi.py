@@ -72,6 +72,7 @@ _SIGNATURES = {
     "bwd_embedding_backward": (
         _int, [_vp, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "bwd_check_device": (_int, [_vp]),
+    "bwd_selftest_bounded_wait": (_int, [_vp]),
     "bwd_status_string": (ctypes.c_char_p, [_int]),
     "bwd_last_error": (ctypes.c_char_p, []),
 }

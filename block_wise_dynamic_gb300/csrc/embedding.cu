@@ -504,6 +504,16 @@ embed_bwd_staged_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, con
   }
 }
 
+// Self-test of the bounded waits: one CTA waits for the first phase of an
+// mbarrier that expects one arrival nobody makes.  Every thread's wait gives
+// up after about a second and the kernel sets the fault word and returns.
+__global__ void __launch_bounds__(32) bounded_wait_selftest_kernel() {
+  __shared__ __align__(8) uint64_t s_bar;
+  if (threadIdx.x == 0) mbar_init(&s_bar, 1);
+  __syncthreads();
+  if (!mbar_wait(&s_bar, 0u) && threadIdx.x == 0) atomicOr(&g_embed_fault, 1u);
+}
+
 // --------------------------------------------------------------------------
 // host side
 
@@ -600,6 +610,14 @@ bwd_status bwd_check_device(void* stream) {
     return cuda_fail(e, "cudaMemcpyToSymbol(fault word)");
   return fail(BWD_ERR_CUDA, "a bounded wait for a bulk copy in a library kernel gave up; the outputs of the "
                             "kernels since the last check are unspecified");
+}
+
+bwd_status bwd_selftest_bounded_wait(void* stream) {
+  EmbedDevice* d = nullptr;
+  bwd_status s = ensure_device(&d);
+  if (s != BWD_OK) return s;
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+  return check_launch("bounded_wait_selftest_kernel launch");
 }
 
 float bwd_embedding_xavier_bound(int64_t num_embeddings, int64_t dim) {

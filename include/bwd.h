@@ -236,6 +236,13 @@ bwd_status bwd_embedding_backward(const int64_t* ids, int64_t num_tokens,
  * Blocking; not callable during stream capture. */
 bwd_status bwd_check_device(void* stream);
 
+/* Self-test of the bounded waits: enqueues one kernel that waits for an
+ * mbarrier phase nothing completes.  Its wait gives up after about a second,
+ * sets the fault word and returns (no trap, the context stays usable); the
+ * next bwd_check_device therefore returns BWD_ERR_CUDA and clears the word.
+ * For tests and diagnostics; no counterpart in the method. */
+bwd_status bwd_selftest_bounded_wait(void* stream);
+
 /* Static description of a status code. */
 const char* bwd_status_string(bwd_status status);
 

@@ -356,3 +356,32 @@ def test_backward_with_many_interleaved_invalid_ids(E):
     t = int(ok.sum())
     for got, ref, s in ((dg, rg, sg), (db, rb, sb)):
         assert np.all(np.abs(got.cpu().numpy() - ref) <= 2 * (128 + t) * U * s + 1e-30)
+
+
+def test_bounded_wait_gives_up_and_is_reported(E):
+    """A wait that nothing completes (the self-test kernel) gives up after
+    about a second, the fault word is reported once and cleared, and the
+    device keeps working."""
+    import time
+
+    import block_wise_dynamic_gb300 as bwd
+    from block_wise_dynamic_gb300 import _abi
+
+    bwd.check_device(0)  # clean start
+    t0 = time.perf_counter()
+    _abi.check(bwd._lib.bwd_selftest_bounded_wait(None), "bwd_selftest_bounded_wait")
+    with pytest.raises(_abi.BwdError) as err:
+        bwd.check_device(0)
+    assert "bounded wait" in str(err.value)
+    assert 0.5 < time.perf_counter() - t0 < 30.0
+    bwd.check_device(0)  # cleared
+    d, v = 256, 50
+    w = torch.from_numpy(rand_weight(v, d, 90)).to(dev())
+    g, b = (torch.from_numpy(a).to(dev()) for a in affine(d, 91))
+    ids = torch.arange(v, device=dev())
+    y, mean, rstd = E.forward(ids, w, g, b)
+    E.backward(ids, w, g, mean, rstd, torch.ones(v, d, device=dev()), torch.zeros_like(w), torch.zeros_like(g),
+               torch.zeros_like(g))
+    bwd.check_device(0)
+    ry, _, _ = se.forward(np.arange(v), w.cpu().numpy(), g.cpu().numpy(), b.cpu().numpy())
+    np.testing.assert_allclose(y.cpu().numpy(), ry, rtol=1e-4, atol=1e-4)
