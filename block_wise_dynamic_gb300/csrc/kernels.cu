@@ -149,22 +149,31 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 }
 
 // Code word of a normalised value (see the bucket entries in tables.h): one
-// table read; the code is the word's top byte.  Signed map: q in [-1, 1]
-// with -0.0 passed as +0.0.  The clamps keep any bit pattern, non-finite ones
-// included, inside the table.
+// table read; the code is the word's top byte.  Signed map, -0.0 passed as
+// +0.0.
+//
+// Range of q.  Every q here is a quotient x / absmax of its own block, and
+// the block absmax is at least every finite |x| of the block (the running
+// maxima start from +0 and max / fmaxf return the non-NaN operand, so no
+// NaN ever reaches them); the quotient is exactly rounded, so |q| <= 1.  A
+// NaN or infinite x makes q a (quiet, as every arithmetic NaN) NaN, or +-0
+// beside an infinite absmax.  So |q| <= 1 or q is a quiet NaN, and the only
+// clamp needed is the lower one, which also sends NaN (fmaxf returns the
+// other operand) to the first bucket: every lookup stays in the table.
 __device__ __forceinline__ uint32_t code_word_signed(float q, const bwd::Tables& tab) {
   const uint32_t b = __float_as_uint(q);
-  const uint32_t h = min(__float_as_uint(fmaxf(fabsf(q), __uint_as_float(bwd::kSgnLo << bwd::kSgnShift))) >>
-                             bwd::kSgnShift, bwd::kSgnHi);
+  const uint32_t h = __float_as_uint(fmaxf(fabsf(q), __uint_as_float(bwd::kSgnLo << bwd::kSgnShift))) >>
+                     bwd::kSgnShift;
   const uint32_t i = h - bwd::kSgnLo + ((b >> 31) ? bwd::kSgnN : 0u);
   const uint32_t low = (b ^ static_cast<uint32_t>(static_cast<int32_t>(b) >> 31)) & bwd::kSgnLowMask;
   return tab.ent[i] + low;
 }
 
-// Unsigned map, q >= +0 (the second moment is never negative).
+// Unsigned map, q in [+0, 1] or NaN (the second moment is never negative;
+// same range argument as above).
 __device__ __forceinline__ uint32_t code_word_unsigned_nonneg(float q, const bwd::Tables& tab) {
   const uint32_t b = __float_as_uint(q);
-  const uint32_t h = min(max(b >> bwd::kUnsShift, bwd::kUnsLo), bwd::kUnsHi);
+  const uint32_t h = __float_as_uint(fmaxf(q, __uint_as_float(bwd::kUnsLo << bwd::kUnsShift))) >> bwd::kUnsShift;
   return tab.ent[bwd::kUnsOff - bwd::kUnsLo + h] + (b & bwd::kUnsLowMask);
 }
 

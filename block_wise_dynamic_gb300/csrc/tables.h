@@ -34,7 +34,10 @@
 //   Unsigned map (second moment): bucket = pattern >> 16 (128 per binade: its
 //   thresholds are 0.7% apart near 1), clamped to [kUnsLo, kUnsHi] (2^-25,
 //   below the smallest threshold 5e-8, to 1.008), from kUnsOff on.
-//   Buckets above 1 exist only as clamp targets: no normalised value is > 1.
+//   Lookups clamp only from below (with fmaxf, which also sends NaN to the
+//   first bucket): a normalised value is a block's own quotient, in [-1, 1]
+//   or NaN (see code_word_signed in kernels.cu), so the bucket of 1.0 is the
+//   top one.
 #pragma once
 
 #include <cstddef>

@@ -441,3 +441,29 @@ def test_f16_param_optimizer(bwd):
     st = opt.state[p]
     compare_bf16_params(p.detach().cpu().view(torch.int16).numpy().view(np.uint16), ref[0])
     assert np.array_equal(st["m_codes"].cpu().numpy(), ref[1]) and np.array_equal(st["v_codes"].cpu().numpy(), ref[3])
+
+
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
+def test_non_finite_gradients_do_not_fault(bwd, gdt):
+    """NaN and infinite gradients (outside the method) in some blocks: the
+    step completes and the other blocks are exactly the oracle's."""
+    n = 5 * B
+    rng = np.random.default_rng(41)
+    p = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    g = (rng.standard_normal(n) * 1e-2).astype(np.float32)
+    g[7] = np.nan
+    g[B + 1000] = np.inf
+    g[2 * B + 3] = -np.inf
+    g[2 * B + 600] = np.nan
+    st = random_state(n, 42)
+    gt = torch.from_numpy(g).to(gdt)
+    dp = torch.from_numpy(p).to(DEV)
+    d = to_dev(*st)
+    bwd.adam8bit_step(dp, gt.to(DEV), *d, lr=1e-3, step=3)
+    torch.cuda.synchronize()
+    hp = oracle.AdamHParams(lr=1e-3, step=3)
+    lo = 3 * B
+    ref = oracle.adam8bit_step(p[lo:], g_to_np(gt)[lo:], st[0][lo:], st[1][3:], st[2][lo:], st[3][3:], hp)
+    got = (dp.cpu().numpy()[lo:], d[0].cpu().numpy()[lo:], d[1].cpu().numpy()[3:], d[2].cpu().numpy()[lo:],
+           d[3].cpu().numpy()[3:])
+    compare_step(got, ref)

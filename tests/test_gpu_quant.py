@@ -229,3 +229,35 @@ def test_tensor_larger_than_2p31_elements(bwd):
         assert np.array_equal(y[lo:hi].cpu().numpy().view(U32), yo.view(U32))
     del x, c, a, y
     torch.cuda.empty_cache()
+
+
+def test_nan_in_another_warp_than_the_block_maximum(bwd):
+    """A NaN and the block's largest finite value in different warps, finite
+    values up to 3e38, an all-NaN block, NaN beside infinity: the maxima
+    ignore NaN, so the absmax is the largest finite magnitude and every
+    finite element gets the oracle's code for the block with the NaN at 0;
+    nothing faults."""
+    B = 2048
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal(6 * B)).astype(np.float32)
+    x[3] = np.nan                      # warp 0 of block 0 (quads 4 t + 512 k + j: thread 0)
+    x[1500] = 3e38                     # a thread of another warp holds the maximum
+    x[B + 700] = -np.nan
+    x[B + 5] = -2.5e38
+    x[2 * B:3 * B] = np.nan            # all NaN
+    x[3 * B + 9] = np.nan
+    x[3 * B + 10] = np.inf             # NaN beside infinity
+    x[4 * B + 2047] = np.nan           # last element
+    for signed in (True, False):
+        with np.errstate(over="ignore"):
+            xs = x if signed else np.where(np.isnan(x), x, x * x).astype(np.float32)
+        c, a = gpu_quant(bwd, xs, signed)
+        for b in (0, 1, 4):
+            blk = xs[b * B:(b + 1) * B]
+            fin = np.isfinite(blk)  # (squares of +-3e38 overflow to infinity on the unsigned side)
+            with np.errstate(invalid="ignore"):  # inf / inf in a block holding an infinity
+                co, ao = oracle.quantize_blockwise(np.where(np.isnan(blk), 0.0, blk).astype(np.float32), signed)
+            assert a[b] == ao[0]
+            assert np.array_equal(c[b * B:(b + 1) * B][fin], co[fin])
+        co, ao = oracle.quantize_blockwise(xs[5 * B:], signed)
+        assert np.array_equal(c[5 * B:], co) and a[5] == ao[0]
