@@ -196,3 +196,35 @@ def test_blockwise_beats_tensorwise_on_outliers():
     yt = m[np.searchsorted(t, x / s, side="right")] * s
     rel_tw = np.abs(yt[B:] - x[B:]).mean() / np.abs(x[B:]).mean()
     assert rel_bw < 0.05 < rel_tw
+
+
+@pytest.mark.parametrize("signed", [True, False])
+def test_codes_are_monotone_within_a_block(signed):
+    """Nearest-entry codes of an ascending map never decrease when the input
+    does: sorting a block's values sorts its codes (a reversed threshold
+    table or a sign slip in the comparison would break this)."""
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal(B) * 10.0 ** rng.uniform(-6, 0, B)).astype(np.float32)
+    if not signed:
+        x = np.abs(x)
+    x.sort()
+    codes, _ = oracle.quantize_blockwise(x, signed)
+    assert np.all(np.diff(codes.astype(np.int32)) >= 0)
+
+
+@pytest.mark.parametrize("signed", [True, False])
+@pytest.mark.parametrize("k", [-40, -7, 1, 30])
+def test_power_of_two_scaling_leaves_codes_unchanged(signed, k):
+    """Scaling a block by 2^k scales every value and the absmax exactly, so
+    x / absmax and the codes are unchanged and the absmax scales by 2^k (a
+    swapped operand in the division or a wrong absmax would show here)."""
+    rng = np.random.default_rng(100 + k)
+    x = (rng.standard_normal(3 * B + 77) * 10.0 ** rng.uniform(-4, 0, 3 * B + 77)).astype(np.float32)
+    if not signed:
+        x = x * x
+    c0, a0 = oracle.quantize_blockwise(x, signed)
+    xs = (x * np.float32(2.0 ** k)).astype(np.float32)
+    assert np.array_equal(xs / np.float32(2.0 ** k), x)  # no value left the normal range
+    c1, a1 = oracle.quantize_blockwise(xs, signed)
+    assert np.array_equal(c0, c1)
+    assert np.array_equal(a1, (a0 * np.float32(2.0 ** k)).astype(np.float32))
