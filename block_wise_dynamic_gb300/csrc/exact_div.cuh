@@ -15,6 +15,19 @@
 // result then still has the right sign and is tiny, but it may differ from
 // RN(x / a) (for instance -0.0 against a negative subnormal).  The tests
 // compare this routine with div.rn over every binary32 significand.
+//
+// Unscaled form (div_unscaled2).  When the divisor's biased exponent lies in
+// [89, 252], that is 2^-38 <= a < 2^126, the scaling can be left out: Y =
+// RN(1 / a) equals y 2^k exactly and is normal, and q0 = RN(x Y), r = x - a q0
+// (one fma), RN(q0 + r Y) take the same values as the scaled sequence times
+// powers of two, so the result is RN(x / a) as long as r is exact.  r is a
+// multiple of 2^(e_a + e_q0 - 46) (e_ the unbiased exponents of a and q0)
+// below 2^(e_a + e_q0 - 22) in magnitude, so it is representable, subnormal
+// or not, whenever e_a + e_q0 >= -103, which |x / a| >= 2^-64 guarantees.
+// Below 2^-64 the unscaled result stays within 2^-22 |x / a| + 2^-111 of x / a
+// (r is then off by at most half a subnormal step, times Y <= 2^38), so its
+// magnitude is below 2^-63, but its sign may differ from that of x.  This
+// saves one multiply per dividend.
 #pragma once
 
 #include <cstdint>
@@ -46,10 +59,10 @@ __device__ __forceinline__ Divisor make_divisor(float d, uint32_t lo_exp) {
 // at half the issue cost.  Measured: a packed multiply whose result feeds a
 // packed add can come out contracted into one fused multiply-add despite
 // the .rn qualifier, so sums of products that must round twice (the Adam
-// moments) stay in scalar __fmul_rn / __fadd_rn; packed operations are used
-// only where no multiply feeds an add (the dequantizing multiply, the exact
-// division, whose products feed fused operations by design, and the
-// approximate parameter update).
+// moments) add in scalar __fadd_rn (their products may be packed); packed
+// adds are used only where no multiply feeds them (the exact division,
+// whose products feed fused operations by design, and the approximate
+// parameter update).
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   float2 d;
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
@@ -87,6 +100,30 @@ __device__ __forceinline__ float2 div_fast2(const Divisor& d, float2 x) {
   const float2 q0 = mul2(xs, dup2(d.y));
   const float2 r = fma2(dup2(-d.a), q0, xs);
   return fma2(r, dup2(d.y), q0);
+}
+
+// Divisors for which div_unscaled2 is exact on quotients of magnitude
+// >= 2^-64 (see the header comment).
+__device__ __forceinline__ bool unscaled_ok(float a) {
+  const uint32_t e = (__float_as_uint(a) >> 23) & 0xffu;
+  return (__float_as_uint(a) >> 31) == 0u && e >= 89u && e <= 252u;
+}
+
+// Y = RN(1 / a) for such a divisor, from its Divisor (exact power-of-two
+// product).
+__device__ __forceinline__ float unscaled_reciprocal(const Divisor& d) { return __fmul_rn(d.y, d.scale); }
+
+__device__ __forceinline__ float div_unscaled(float x, float a, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-a, q0, x);
+  return __fmaf_rn(r, y, q0);
+}
+
+__device__ __forceinline__ float2 div_unscaled2(float2 x, float a, float y) {
+  const float2 y2 = dup2(y);
+  const float2 q0 = mul2(x, y2);
+  const float2 r = fma2(dup2(-a), q0, x);
+  return fma2(r, y2, q0);
 }
 
 }  // namespace bwd

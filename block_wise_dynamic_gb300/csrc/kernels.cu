@@ -31,7 +31,7 @@
 // the threshold compare (an integer compare of pattern bits inside a bucket,
 // the same decision for every binary32 value; tables.h).  The moments use
 // the same operations, in the same order, as the CPU oracle; the parameter
-// update uses approximate rsqrt / rcp (a few ulps of the update term).
+// update uses approximate sqrt / rcp (a few ulps of the update term).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -91,6 +91,11 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 __device__ __forceinline__ float max3abs(float a, float b, float c) {
   float d;
   asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3abs(float a, float b, float c) {
+  float d;
+  asm("min.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 
@@ -193,6 +198,17 @@ __device__ __forceinline__ uint32_t code_word_unsigned(float q, const bwd::Table
 // min over the quotients flags a block that has one (a -0.0 quotient
 // included); its values with the sign bit set are then redone with IEEE
 // division, and a zero quotient is looked up as +0.0.
+//
+// The fused step's moments (kAnySign false: m of any sign, v >= 0) take the
+// unscaled division when the absmax allows it (2^-38 <= a < 2^126), exact
+// for quotients of magnitude >= 2^-64; smaller ones come out below 2^-63 in
+// magnitude with a sign that may be wrong.  For m a three-input min of
+// magnitudes flags a block with a quotient below 2^-63, and there every
+// value with |RN(x Y)| < 2^-62 (every true quotient below 2^-64 among them)
+// is redone with IEEE division.  v needs no check: all thresholds of the
+// unsigned map lie above 2^-25, and any quotient below that, of either sign,
+// is looked up in the first bucket, which holds no threshold (checked when
+// the tables are built), so it gets code 0 like every true quotient there.
 template <bool kSigned, bool kAnySign>
 __device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, const bwd::Tables& tab,
                                                uint32_t (&w)[kQuads]) {
@@ -202,7 +218,23 @@ __device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, 
     for (int j = 0; j < kPer; ++j) c[j] = kSigned ? (128u << 24) : 0u;
   } else {
     const bwd::Divisor d = bwd::make_divisor(a, 1u);
-    if (d.fast) {
+    if (!kAnySign && bwd::unscaled_ok(a)) {
+      const float y = bwd::unscaled_reciprocal(d);
+      float mq = 1.0f;  // smallest quotient magnitude (m only)
+#pragma unroll
+      for (int j = 0; j < kPer; j += 2) {
+        const float2 q = bwd::div_unscaled2(make_float2(x[j], x[j + 1]), a, y);
+        if (kSigned) mq = min3abs(mq, q.x, q.y);
+        c[j] = kSigned ? code_word_signed(q.x, tab) : code_word_unsigned_nonneg(q.x, tab);
+        c[j + 1] = kSigned ? code_word_signed(q.y, tab) : code_word_unsigned_nonneg(q.y, tab);
+      }
+      if (kSigned && mq < 0x1p-63f) {
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+          if (fabsf(__fmul_rn(x[j], y)) < 0x1p-62f)
+            c[j] = code_word_signed(__fadd_rn(__fdiv_rn(x[j], a), 0.0f), tab);  // -0.0 -> +0.0
+      }
+    } else if (d.fast) {
       int minb = 0x7fffffff;
 #pragma unroll
       for (int j = 0; j < kPer; j += 2) {
@@ -424,11 +456,12 @@ __device__ __forceinline__ void load4(const void* base, int64_t e, float* out) {
   }
 }
 
-// Branch-free approximate reciprocal square root and reciprocal (PTX
-// rsqrt.approx / rcp.approx, a few ulps; inputs here are normal numbers).
-__device__ __forceinline__ float rsqrt_approx(float x) {
+// Branch-free approximate square root and reciprocal (PTX sqrt.approx /
+// rcp.approx, a few ulps; a subnormal v counts as 0, which leaves eps alone
+// in the denominator).
+__device__ __forceinline__ float sqrt_approx(float x) {
   float r;
-  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
@@ -453,6 +486,16 @@ template <int kT>
 __device__ __forceinline__ uint32_t bits16(float x) {
   if (kT == kBF16) return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
   return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(x)));
+}
+
+// Two values as a packed pair of bf16 or fp16 values (lo in the low half),
+// each rounded to nearest even: one conversion instruction per pair.
+template <int kT>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  uint32_t r;
+  if (kT == kBF16) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // kG: gradient type; kP: parameter type (kF32, kBF16 or kF16; 16-bit
@@ -552,24 +595,23 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
     // of the update term)
     float m[kPer], v[kPer];
     float mx[2] = {0.0f, 0.0f};
-    const float2 ma2 = bwd::dup2(ma_old), va2 = bwd::dup2(va_old), tiny2 = bwd::dup2(1e-37f), ic2 = bwd::dup2(inv_bc2s);
+    const float2 ma2 = bwd::dup2(ma_old), va2 = bwd::dup2(va_old), ic2 = bwd::dup2(inv_bc2s);
+    const float2 b1_2 = bwd::dup2(b1), omb1_2 = bwd::dup2(omb1), b2_2 = bwd::dup2(b2), omb2_2 = bwd::dup2(omb2);
     const float2 eps2 = bwd::dup2(eps), nstep2 = bwd::dup2(-step_size), decay2 = bwd::dup2(decay);
 #pragma unroll
     for (int j = 0; j < kPer; j += 2) {
       const float2 mo = bwd::mul2(make_float2(map_s[byte_of(mw[j >> 2], j & 3)], map_s[byte_of(mw[j >> 2], (j & 3) + 1)]), ma2);
       const float2 vo = bwd::mul2(make_float2(map_u[byte_of(vw[j >> 2], j & 3)], map_u[byte_of(vw[j >> 2], (j & 3) + 1)]), va2);
       const float2 g2 = make_float2(g[j], g[j + 1]);
-      // the moments stay scalar: a packed multiply feeding a packed add may be
-      // contracted into one fused operation, which would change the rounding
-      const float2 mm = make_float2(__fadd_rn(__fmul_rn(b1, mo.x), __fmul_rn(omb1, g2.x)),
-                                    __fadd_rn(__fmul_rn(b1, mo.y), __fmul_rn(omb1, g2.y)));
-      const float2 vv = make_float2(__fadd_rn(__fmul_rn(b2, vo.x), __fmul_rn(__fmul_rn(omb2, g2.x), g2.x)),
-                                    __fadd_rn(__fmul_rn(b2, vo.y), __fmul_rn(__fmul_rn(omb2, g2.y), g2.y)));
+      // products packed, sums scalar: a packed multiply feeding a packed add
+      // may be contracted into one fused operation, which would change the
+      // rounding
+      const float2 bm = bwd::mul2(b1_2, mo), gm = bwd::mul2(omb1_2, g2);
+      const float2 bv = bwd::mul2(b2_2, vo), gv = bwd::mul2(bwd::mul2(omb2_2, g2), g2);
+      const float2 mm = make_float2(__fadd_rn(bm.x, gm.x), __fadd_rn(bm.y, gm.y));
+      const float2 vv = make_float2(__fadd_rn(bv.x, gv.x), __fadd_rn(bv.y, gv.y));
       m[j] = mm.x; m[j + 1] = mm.y; v[j] = vv.x; v[j + 1] = vv.y;
-      // sqrt(v) = v * rsqrt(v); the 1e-37 keeps rsqrt finite at v = 0
-      const float2 vt = bwd::add2(vv, tiny2);
-      const float2 rs = make_float2(rsqrt_approx(vt.x), rsqrt_approx(vt.y));
-      const float2 den = bwd::fma2(bwd::mul2(vv, rs), ic2, eps2);
+      const float2 den = bwd::fma2(make_float2(sqrt_approx(vv.x), sqrt_approx(vv.y)), ic2, eps2);
       const float2 rc = make_float2(rcp_approx(den.x), rcp_approx(den.y));
       const float2 pp = bwd::fma2(bwd::mul2(nstep2, mm), rc, bwd::mul2(make_float2(p[j], p[j + 1]), decay2));
       p[j] = pp.x; p[j + 1] = pp.y;
@@ -582,8 +624,7 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
         const int64_t e = base + kSpan * k + 4 * t;
         if (kP != kF32)
           __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(T.p) + e),
-                 make_uint2(bits16<kP>(p[4 * k]) | (bits16<kP>(p[4 * k + 1]) << 16),
-                            bits16<kP>(p[4 * k + 2]) | (bits16<kP>(p[4 * k + 3]) << 16)));
+                 make_uint2(pack16<kP>(p[4 * k], p[4 * k + 1]), pack16<kP>(p[4 * k + 2], p[4 * k + 3])));
         else
           __stcs(reinterpret_cast<float4*>(static_cast<float*>(T.p) + e),
                  make_float4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]));

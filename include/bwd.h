@@ -130,7 +130,7 @@ bwd_status bwd_state_init(uint8_t* m_codes, float* m_absmax, uint8_t* v_codes,
  * m and v block by block with fresh absmax.  m and v take one binary32
  * rounding per operation in that order, so the new codes and absmax are
  * exactly those of IEEE arithmetic; the parameter update uses approximate
- * (rsqrt / rcp) arithmetic and is within a few ulps of the update term.
+ * (sqrt / rcp) arithmetic and is within a few ulps of the update term.
  *   p                : device float[n], updated in place.
  *   g                : device, float[n], bf16[n] or fp16[n] per g_dtype, read
  *                      only.

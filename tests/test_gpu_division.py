@@ -1,10 +1,11 @@
 """The per-block division used by the quantizers (exact_div.cuh, scalar and
-packed-pair forms: a correctly rounded reciprocal plus Markstein's
-correction) against the GPU's IEEE division, bit for bit.  The full run over all 2^23 divisor significands
-(about 90 s) is exhaustive; here the first and last 16,384 divisor
-significands (the last ones include the all-ones significand) are checked
-against every dividend significand of both signs, plus 1.6e10 random pairs
-over the exponent range."""
+packed-pair forms, scaled and unscaled: a correctly rounded reciprocal plus
+Markstein's correction) against the GPU's IEEE division, bit for bit.  The
+full run over all 2^23 divisor significands (about 90 s) is exhaustive; here
+the first and last 16,384 divisor significands (the last ones include the
+all-ones significand) are checked against every dividend significand of both
+signs, plus 1.6e10 random pairs over the exponent range, plus the unscaled
+form at both ends of its divisor range with quotients around 2^-64."""
 
 import os
 import shutil
@@ -33,4 +34,6 @@ def test_fast_division_is_ieee_division(div_check, first):
     r = subprocess.run([div_check, "16384", str(first)], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "part1: divisor significands 16384, checked 274877906944, mismatches 0" in r.stdout
-    assert "mismatches 0" in r.stdout.splitlines()[1]
+    lines = r.stdout.splitlines()
+    assert lines[1].startswith("part2:") and lines[1].endswith("mismatches 0")
+    assert lines[2].startswith("part3:") and lines[2].endswith("mismatches 0")
