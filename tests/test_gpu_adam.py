@@ -467,3 +467,42 @@ def test_non_finite_gradients_do_not_fault(bwd, gdt):
     got = (dp.cpu().numpy()[lo:], d[0].cpu().numpy()[lo:], d[1].cpu().numpy()[3:], d[2].cpu().numpy()[lo:],
            d[3].cpu().numpy()[3:])
     compare_step(got, ref)
+
+
+def test_tiny_quotients_across_the_divisor_range(bwd):
+    """Blocks whose new m or v absmax sits at either side of 2^-38 (where the
+    kernel switches between the scaled and unscaled exact divisions) or far
+    from it, each holding quotients down to 2^-80, signed zeros and
+    subnormals: codes and absmax bit-identical to the oracle over two steps."""
+    rng = np.random.default_rng(77)
+    m_edge = 2.0 ** -38 * 10.0  # |g| giving m = 0.1 g at 2^-38 on the first step
+    v_edge = np.sqrt(2.0 ** -38 * 1000.0)  # |g| giving v = 0.001 g^2 at 2^-38
+    tops = [1.2 * m_edge, 0.6 * m_edge, 1.01 * m_edge, 0.99 * m_edge, 1.1 * v_edge, 0.8 * v_edge,
+            1e-30, 1e-20, 1e-3, 1.0, 1e10]
+    tops += list(2.0 ** rng.uniform(-60, 20, 21))
+    blocks = []
+    for top in tops:
+        blk = rng.standard_normal(B)
+        blk *= top / np.abs(blk).max()
+        k = rng.integers(0, B, 300)
+        blk[k] = rng.choice([-1.0, 1.0], 300) * 2.0 ** rng.uniform(-80, -40, 300) * top
+        blk[rng.integers(0, B, 8)] = -0.0
+        blk[rng.integers(0, B, 8)] = 0.0
+        blocks.append(blk)
+    g = np.concatenate(blocks).astype(np.float32)
+    n = g.size
+    p = np.zeros(n, np.float32)
+    dp, dg = to_dev(p, g)
+    st = [t for t in to_dev(*oracle.state_init(n))]
+    ref = (p.copy(), *oracle.state_init(n))
+    for t in (1, 2):
+        gt = g if t == 1 else np.roll(g, 977)
+        dg.copy_(torch.from_numpy(gt))
+        bwd.adam8bit_step(dp, dg, *st, lr=1e-3, step=t)
+        ref = oracle.adam8bit_step(ref[0], gt, *ref[1:], oracle.AdamHParams(lr=1e-3, step=t))
+        torch.cuda.synchronize()
+        if t == 1:  # both sides of the switch, for m and for v
+            for a in (ref[2], ref[4]):
+                assert {88, 89} <= set(((a.view(U32) >> 23) & 0xFF).tolist())
+        for a, b in zip((x.cpu().numpy() for x in st), ref[1:]):
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
