@@ -385,3 +385,61 @@ def test_bounded_wait_gives_up_and_is_reported(E):
     bwd.check_device(0)
     ry, _, _ = se.forward(np.arange(v), w.cpu().numpy(), g.cpu().numpy(), b.cpu().numpy())
     np.testing.assert_allclose(y.cpu().numpy(), ry, rtol=1e-4, atol=1e-4)
+
+
+@pytest.mark.parametrize("shape", [(0,), (3, 0)])
+def test_zero_tokens_are_no_ops(E, shape):
+    d, v = 256, 40
+    w = torch.from_numpy(rand_weight(v, d, 12)).to(dev())
+    g, b = (torch.from_numpy(a).to(dev()) for a in affine(d, 13))
+    ids = torch.zeros(shape, dtype=torch.int64, device=dev())
+    y, mean, rstd = E.forward(ids, w, g, b)
+    assert tuple(y.shape) == shape + (d,) and mean.numel() == 0 and rstd.numel() == 0
+    dw = torch.full_like(w, 0.5)
+    dg = torch.full_like(g, 0.25)
+    db = torch.full_like(g, -1.0)
+    E.backward(ids.reshape(-1), w, g, mean, rstd, y.reshape(0, d), dw, dg, db)
+    torch.cuda.synchronize()
+    assert torch.all(dw == 0.5) and torch.all(dg == 0.25) and torch.all(db == -1.0)
+
+
+def test_weight_larger_than_2p31_elements(E):
+    """A 600,000 x 4,096 weight (2.46e9 elements, offsets past 2^31): tokens
+    whose rows lie beyond element 2^31, and rows on both sides of it, against
+    the oracle on those rows (forward, and backward into the weight's
+    gradient)."""
+    from block_wise_dynamic_gb300 import workloads as W
+
+    v, d = 600_000, 4096
+    w = torch.empty(v, d, dtype=torch.float32, device=dev())
+    E.init_weight(w, None, generator=torch.Generator(device=dev()).manual_seed(5))
+    edge = (1 << 31) // d  # first row starting at element 2^31
+    rows = np.array([0, 1, v // 2 + 17, edge - 1, edge, edge + 1, v - 2, v - 1], dtype=np.int64)  # ascending
+    assert np.all(np.diff(rows) > 0)
+    rng = np.random.default_rng(63)
+    idn = rows[rng.integers(0, rows.size, 600)]
+    ids = torch.from_numpy(idn).to(dev())
+    gamma, beta = affine(d, 64)
+    g_d, b_d = torch.from_numpy(gamma).to(dev()), torch.from_numpy(beta).to(dev())
+    y, mean, rstd = E.forward(ids, w, g_d, b_d)
+    dy = W.gen_normal(idn.size * d, 1.0, seed=65, device=dev()).view(idn.size, d)
+    dw = torch.zeros_like(w)
+    dg = torch.zeros_like(g_d)
+    db = torch.zeros_like(g_d)
+    E.backward(ids, w, g_d, mean, rstd, dy, dw, dg, db)
+    torch.cuda.synchronize()
+    sub = w[torch.from_numpy(rows).to(dev())].cpu().numpy()
+    local = np.searchsorted(rows, idn)  # index of each token's row in `rows`
+    assert np.array_equal(rows[local], idn)
+    ry, _, _ = se.forward(local, sub, gamma, beta)
+    x = sub[local].astype(np.float64)
+    xhat = (x - x.mean(axis=1, keepdims=True)) / np.sqrt(x.var(axis=1, keepdims=True) + se.EPS)
+    tol = 640 * U * (1 + np.abs(xhat)) * np.abs(gamma) + 4 * U * np.abs(beta)
+    assert np.all(np.abs(y.cpu().numpy() - ry) <= tol)
+    dyn = dy.cpu().numpy().astype(np.float64)
+    rw, _, _ = se.backward(local, sub, gamma, dyn)
+    sw, _, _ = se.backward_abs_sums(local, sub, gamma, dyn)
+    k = np.bincount(local, minlength=rows.size)[:, None]
+    got = dw[torch.from_numpy(rows).to(dev())].cpu().numpy()
+    assert np.all(np.abs(got - rw) <= 2 * (128 + k) * U * sw + 1e-30)
+    assert float(dw[2].abs().max()) == 0.0 and float(dw[edge + 2].abs().max()) == 0.0
