@@ -103,15 +103,12 @@ __device__ __forceinline__ float2 div_fast2(const Divisor& d, float2 x) {
 }
 
 // Divisors for which div_unscaled2 is exact on quotients of magnitude
-// >= 2^-64 (see the header comment).
+// >= 2^-64 (see the header comment): positive, exponent field in [89, 252],
+// one unsigned compare.  Their reciprocal Y = RN(1 / a) (__frcp_rn) is
+// normal.
 __device__ __forceinline__ bool unscaled_ok(float a) {
-  const uint32_t e = (__float_as_uint(a) >> 23) & 0xffu;
-  return (__float_as_uint(a) >> 31) == 0u && e >= 89u && e <= 252u;
+  return __float_as_uint(a) - (89u << 23) < ((253u - 89u) << 23);
 }
-
-// Y = RN(1 / a) for such a divisor, from its Divisor (exact power-of-two
-// product).
-__device__ __forceinline__ float unscaled_reciprocal(const Divisor& d) { return __fmul_rn(d.y, d.scale); }
 
 __device__ __forceinline__ float div_unscaled(float x, float a, float y) {
   const float q0 = __fmul_rn(x, y);

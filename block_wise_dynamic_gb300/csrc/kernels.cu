@@ -213,28 +213,28 @@ template <bool kSigned, bool kAnySign>
 __device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, const bwd::Tables& tab,
                                                uint32_t (&w)[kQuads]) {
   uint32_t c[kPer];  // code words (code in the top byte)
-  if (a == 0.0f) {
+  if (!kAnySign && bwd::unscaled_ok(a)) {
+    const float y = __frcp_rn(a);  // RN(1 / a), a normal number for such a
+    float mq = 1.0f;               // smallest quotient magnitude (m only)
+#pragma unroll
+    for (int j = 0; j < kPer; j += 2) {
+      const float2 q = bwd::div_unscaled2(make_float2(x[j], x[j + 1]), a, y);
+      if (kSigned) mq = min3abs(mq, q.x, q.y);
+      c[j] = kSigned ? code_word_signed(q.x, tab) : code_word_unsigned_nonneg(q.x, tab);
+      c[j + 1] = kSigned ? code_word_signed(q.y, tab) : code_word_unsigned_nonneg(q.y, tab);
+    }
+    if (kSigned && mq < 0x1p-63f) {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j)
+        if (fabsf(__fmul_rn(x[j], y)) < 0x1p-62f)
+          c[j] = code_word_signed(__fadd_rn(__fdiv_rn(x[j], a), 0.0f), tab);  // -0.0 -> +0.0
+    }
+  } else if (a == 0.0f) {
 #pragma unroll
     for (int j = 0; j < kPer; ++j) c[j] = kSigned ? (128u << 24) : 0u;
   } else {
     const bwd::Divisor d = bwd::make_divisor(a, 1u);
-    if (!kAnySign && bwd::unscaled_ok(a)) {
-      const float y = bwd::unscaled_reciprocal(d);
-      float mq = 1.0f;  // smallest quotient magnitude (m only)
-#pragma unroll
-      for (int j = 0; j < kPer; j += 2) {
-        const float2 q = bwd::div_unscaled2(make_float2(x[j], x[j + 1]), a, y);
-        if (kSigned) mq = min3abs(mq, q.x, q.y);
-        c[j] = kSigned ? code_word_signed(q.x, tab) : code_word_unsigned_nonneg(q.x, tab);
-        c[j + 1] = kSigned ? code_word_signed(q.y, tab) : code_word_unsigned_nonneg(q.y, tab);
-      }
-      if (kSigned && mq < 0x1p-63f) {
-#pragma unroll
-        for (int j = 0; j < kPer; ++j)
-          if (fabsf(__fmul_rn(x[j], y)) < 0x1p-62f)
-            c[j] = code_word_signed(__fadd_rn(__fdiv_rn(x[j], a), 0.0f), tab);  // -0.0 -> +0.0
-      }
-    } else if (d.fast) {
+    if (d.fast) {
       int minb = 0x7fffffff;
 #pragma unroll
       for (int j = 0; j < kPer; j += 2) {

@@ -70,8 +70,7 @@ __global__ void part3(uint32_t a_lo, uint32_t ea, int dq) {
   const uint32_t ai = a_lo + blockIdx.y;
   if (ai >= (1u << 23)) return;
   const float a = __uint_as_float((ea << 23) | ai);
-  const bwd::Divisor d = bwd::make_divisor(a, 1);
-  const float y = bwd::unscaled_reciprocal(d);
+  const float y = __frcp_rn(a);
   const uint32_t ex = static_cast<uint32_t>(static_cast<int>(ea) + dq);
   unsigned long long bad = 0, n = 0;
   if (!bwd::unscaled_ok(a)) {
@@ -110,7 +109,7 @@ __global__ void part2(uint32_t seed, uint32_t iters) {
     const bwd::Divisor d = bwd::make_divisor(a, 1);
     if (bwd::unscaled_ok(a)) {
       ++n;
-      if (!check_unscaled(x, a, bwd::unscaled_reciprocal(d), e)) { ++bad; record(x, a); }
+      if (!check_unscaled(x, a, __frcp_rn(a), e)) { ++bad; record(x, a); }
     }
     if (fabsf(e) < 0x1p-64f) continue;
     if (!d.fast) continue;
