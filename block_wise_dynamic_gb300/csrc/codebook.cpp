@@ -133,11 +133,12 @@ int build_entries(const float* ts, const float* tu, uint32_t* ent, char* err, si
                    &ent[kUnsOff + h - kUnsLo], err, errlen) != 0)
       return -1;
   }
-  // The fused step divides v by its block absmax without the tiny-quotient
-  // check (exact_div.cuh, unscaled form), so a quotient below 2^-63 may come
-  // out with either sign; the unsigned lookup then reads the first bucket's
-  // entry with arbitrary low bits.  That gives code 0, the code of every such
-  // quotient, only while the first bucket holds no threshold.
+  // Unsigned quantization divides by the block absmax without a
+  // tiny-quotient check (exact_div.cuh, unscaled form), so a quotient below
+  // 2^-63 may come out with either sign; the non-negative lookup then reads
+  // the first bucket's entry with arbitrary low bits.  That gives code 0, the
+  // code of every such quotient, only while the first bucket holds no
+  // threshold.
   if (ent[kUnsOff] != (1u << kEntShift) - (1u << kSgnShift)) {
     std::snprintf(err, errlen, "the first unsigned bucket holds a threshold");
     return -1;

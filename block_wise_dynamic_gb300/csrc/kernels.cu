@@ -199,29 +199,30 @@ __device__ __forceinline__ uint32_t code_word_unsigned(float q, const bwd::Table
 // included); its values with the sign bit set are then redone with IEEE
 // division, and a zero quotient is looked up as +0.0.
 //
-// The fused step's moments (kAnySign false: m of any sign, v >= 0) take the
-// unscaled division when the absmax allows it (2^-38 <= a < 2^126), exact
+// An absmax in [2^-38, 2^126) takes the unscaled division instead, exact
 // for quotients of magnitude >= 2^-64; smaller ones come out below 2^-63 in
-// magnitude with a sign that may be wrong.  For m a three-input min of
-// magnitudes flags a block with a quotient below 2^-63, and there every
-// value with |RN(x Y)| < 2^-62 (every true quotient below 2^-64 among them)
-// is redone with IEEE division.  v needs no check: all thresholds of the
-// unsigned map lie above 2^-25, and any quotient below that, of either sign,
-// is looked up in the first bucket, which holds no threshold (checked when
-// the tables are built), so it gets code 0 like every true quotient there.
+// magnitude with a sign that may be wrong.  For the signed map a
+// three-input min of magnitudes flags a block with a quotient below 2^-63,
+// and there every value with |RN(x Y)| < 2^-62 (every true quotient below
+// 2^-64 among them) is redone with IEEE division.  The unsigned map needs
+// no check: all its thresholds lie above 2^-25, a negative quotient has
+// code 0 (any-sign lookup), and a non-negative lookup of a value below
+// 2^-25, of either sign, reads the first bucket, which holds no threshold
+// (checked when the tables are built) and so gives code 0, the code of
+// every true quotient there.
 template <bool kSigned, bool kAnySign>
 __device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, const bwd::Tables& tab,
                                                uint32_t (&w)[kQuads]) {
   uint32_t c[kPer];  // code words (code in the top byte)
-  if (!kAnySign && bwd::unscaled_ok(a)) {
+  if (bwd::unscaled_ok(a)) {
     const float y = __frcp_rn(a);  // RN(1 / a), a normal number for such a
     float mq = 1.0f;               // smallest quotient magnitude (m only)
 #pragma unroll
     for (int j = 0; j < kPer; j += 2) {
       const float2 q = bwd::div_unscaled2(make_float2(x[j], x[j + 1]), a, y);
       if (kSigned) mq = min3abs(mq, q.x, q.y);
-      c[j] = kSigned ? code_word_signed(q.x, tab) : code_word_unsigned_nonneg(q.x, tab);
-      c[j + 1] = kSigned ? code_word_signed(q.y, tab) : code_word_unsigned_nonneg(q.y, tab);
+      c[j] = kSigned ? code_word_signed(q.x, tab) : (kAnySign ? code_word_unsigned(q.x, tab) : code_word_unsigned_nonneg(q.x, tab));
+      c[j + 1] = kSigned ? code_word_signed(q.y, tab) : (kAnySign ? code_word_unsigned(q.y, tab) : code_word_unsigned_nonneg(q.y, tab));
     }
     if (kSigned && mq < 0x1p-63f) {
 #pragma unroll
