@@ -261,3 +261,33 @@ def test_nan_in_another_warp_than_the_block_maximum(bwd):
             assert np.array_equal(c[b * B:(b + 1) * B][fin], co[fin])
         co, ao = oracle.quantize_blockwise(xs[5 * B:], signed)
         assert np.array_equal(c[5 * B:], co) and a[5] == ao[0]
+
+
+@pytest.mark.parametrize("signed", [True, False])
+def test_tiny_quotients_on_both_sides_of_the_unscaled_switch(bwd, signed):
+    """Block absmax just below and above 2^-38 and 2^126 (where the
+    quantizers switch between the unscaled and scaled exact divisions) and
+    elsewhere, each block holding quotients down to 2^-80 of both signs,
+    signed zeros and subnormals (the unsigned map sees negative values too):
+    codes and absmax bit-identical to the oracle."""
+    B = 2048
+    rng = np.random.default_rng(23)
+    tops = [2.0 ** -38 * f for f in (0.6, 0.99, 1.0, 1.01, 1.5)]
+    tops += [2.0 ** 126 * f for f in (0.9, 0.99, 1.0, 1.5)]
+    tops += list(2.0 ** rng.uniform(-120, 120, 16))
+    rows = []
+    for top in tops:
+        r = rng.standard_normal(B)
+        r *= top / np.abs(r).max()
+        k = rng.integers(0, B, 400)
+        r[k] = rng.choice([-1.0, 1.0], 400) * 2.0 ** rng.uniform(-80, -30, 400) * top
+        r[rng.integers(0, B, 8)] = -0.0
+        r[rng.integers(0, B, 8)] = 0.0
+        rows.append(r.astype(np.float32))
+    x = np.concatenate(rows)
+    fields = (np.abs(x).reshape(-1, B).max(axis=1).view(U32) >> 23) & 0xFF
+    assert {88, 89, 252, 253} <= set(fields.tolist())
+    c, a = gpu_quant(bwd, x, signed)
+    co, ao = oracle.quantize_blockwise(x, signed)
+    assert np.array_equal(a.view(U32), ao.view(U32))
+    assert np.array_equal(c, co)
