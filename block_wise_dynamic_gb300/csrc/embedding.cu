@@ -372,7 +372,13 @@ embed_bwd_staged_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, con
   extern __shared__ __align__(128) float s_buf[];  // [group][buffer][x | dy][dim]
   __shared__ __align__(16) float s_red[kSGroups][2 * 2 * kSGWarps];
   __shared__ __align__(8) uint64_t s_full[kSGroups][2];
-  __shared__ int s_abort[kSGroups];
+  // s_abort[group][c]: a wait gave up in an iteration of parity 1 - c.  All
+  // threads read cell (it & 1) right after the loop-top barrier of
+  // iteration it.  Writes to that cell come from iteration it - 1, finished
+  // before that barrier, or from iteration it + 1, which no thread enters
+  // before every thread has reached the next loop-top barrier, after its
+  // read: so all threads of the group decide alike.
+  __shared__ int s_abort[kSGroups][2];
   const int group = threadIdx.x / kSG, t = threadIdx.x % kSG;
   const int nch = dim >> 2;
   const float fdim = static_cast<float>(dim);
@@ -381,7 +387,7 @@ embed_bwd_staged_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, con
   if (t == 0) {
     mbar_init(&s_full[group][0], 1);
     mbar_init(&s_full[group][1], 1);
-    s_abort[group] = 0;
+    s_abort[group][0] = s_abort[group][1] = 0;
   }
   __syncthreads();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kSGroups;
@@ -410,7 +416,7 @@ embed_bwd_staged_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, con
   for (int64_t tok = tok0; tok < num_tokens; tok += stride, ++it) {
     const int b = it & 1;
     group_sync256(group);  // every thread is done with the other buffer
-    if (s_abort[group]) break;
+    if (s_abort[group][it & 1]) break;
     if (t == 0 && tok + stride < num_tokens) issue(tok + stride, b ^ 1);
     const int64_t id = ids[tok];
     if (id < 0 || id >= vocab) continue;  // the whole group skips together
@@ -418,7 +424,7 @@ embed_bwd_staged_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, con
     phase ^= 1u << b;
     if (!ok) {
       atomicOr(&g_embed_fault, 1u);
-      s_abort[group] = 1;
+      s_abort[group][(it + 1) & 1] = 1;
     }
     {
       const int64_t nx = tok + stride;
@@ -479,7 +485,7 @@ embed_bwd_staged_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, con
   }
   // a group that gave up lets its copy in flight land (bounded) before the
   // buffers are reused below
-  if (t == 0 && pending >= 0 && s_abort[group]) mbar_wait(&s_full[group][pending], (phase >> pending) & 1u);
+  if (t == 0 && pending >= 0 && (s_abort[group][0] || s_abort[group][1])) mbar_wait(&s_full[group][pending], (phase >> pending) & 1u);
   __syncthreads();
   // partials: each group's into its first buffer, then summed over the groups in order
   float* const part = s_buf + static_cast<int64_t>(group) * 4 * dim;
