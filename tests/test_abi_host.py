@@ -173,3 +173,27 @@ def test_pointers_misaligned_for_their_element_size_are_rejected(lib):
     assert lib.bwd_embedding_forward(ctypes.c_void_p(0x1004), 10, ok, 100, 64, ok, ok, 1e-5, ok, None, None,
                                      None) == 1
     assert lib.bwd_embedding_init(ok, 4, 4, two, None) == 1
+
+
+def test_missing_library_fails_loudly():
+    """Without the built library every call raises ImportError: there is no
+    CPU fallback behind the package's functions."""
+    import subprocess
+    import sys
+
+    code = (
+        "import block_wise_dynamic_gb300._abi as a\n"
+        "a.LIB_PATH = '/nonexistent/libbwd.so'\n"
+        "import block_wise_dynamic_gb300 as m\n"
+        "from block_wise_dynamic_gb300 import embedding as emb\n"
+        "for call in (lambda: m.build_map('signed'), lambda: emb.xavier_bound(10, 10)):\n"
+        "    try:\n"
+        "        call()\n"
+        "    except ImportError as err:\n"
+        "        assert 'no fallback' in str(err)\n"
+        "    else:\n"
+        "        raise SystemExit('no ImportError')\n"
+        "print('ok')\n"
+    )
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
