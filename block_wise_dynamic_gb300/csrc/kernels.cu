@@ -351,21 +351,39 @@ quantize_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ co
 
 // --------------------------------------------------------------------------
 // dequantize (256 threads, 8 elements per thread: 4 t + j and 1024 + 4 t + j)
+//
+// A full block's 8 KB of output is assembled in shared memory and written by
+// one bulk copy (cp.async.bulk, shared -> global) that thread 0 issues; three
+// buffers rotate, so up to two blocks' stores are in flight while the next
+// block is computed.  Before a buffer is refilled, thread 0 waits until at
+// most two bulk groups still read shared memory (cp.async.bulk.wait_group.read:
+// a wait on the CTA's own copies, which always complete) and the CTA meets at
+// a barrier.  The stream is write-heavy (4 bytes written per byte read); the
+// bulk stores reach a higher DRAM rate than per-thread 16-byte stores.
+// Partial blocks and unaligned buffers take element-wise stores.
+
+constexpr int kDeqBufs = 3;
 
 template <bool kSigned>
 __global__ void __launch_bounds__(kDeqThreads)
 dequantize_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ absmax, int64_t n,
                   float* __restrict__ y, int vec_ok) {
   __shared__ __align__(16) float s_map[kCodes];
+  __shared__ __align__(128) float s_out[kDeqBufs][BWD_BLOCK];
   copy_to_smem(s_map, g_tables.map[kSigned ? 0 : 1], sizeof(s_map));
   __syncthreads();
   const int tid = threadIdx.x;
   const int64_t nb = (n + BWD_BLOCK - 1) / BWD_BLOCK;
+  int buf_i = 0;
   for (int64_t b = blockIdx.x; b < nb; b += gridDim.x) {
     const int64_t base = b * BWD_BLOCK;
     const int rem = static_cast<int>(rem_in_block(n, base));
     const float am = absmax[b];
     if (vec_ok && rem == BWD_BLOCK) {
+      float* buf = s_out[buf_i];
+      buf_i = (buf_i == kDeqBufs - 1) ? 0 : buf_i + 1;
+      if (tid == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kDeqBufs - 1) : "memory");
+      __syncthreads();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(codes + base + 1024 * h) + tid);
@@ -374,7 +392,17 @@ dequantize_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ a
         o.y = __fmul_rn(s_map[byte_of(w, 1)], am);
         o.z = __fmul_rn(s_map[byte_of(w, 2)], am);
         o.w = __fmul_rn(s_map[byte_of(w, 3)], am);
-        __stcs(reinterpret_cast<float4*>(y + base + 1024 * h) + tid, o);
+        reinterpret_cast<float4*>(buf + 1024 * h)[tid] = o;
+      }
+      // The generic-proxy writes above become visible to the bulk copy.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncthreads();
+      if (tid == 0) {
+        const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(buf));
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(y + base), "r"(sa),
+                     "n"(BWD_BLOCK * 4)
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
     } else {
 #pragma unroll
@@ -384,6 +412,8 @@ dequantize_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ a
       }
     }
   }
+  // Shared memory must outlive the bulk copies that read it.
+  if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // --------------------------------------------------------------------------
