@@ -290,6 +290,45 @@ __device__ __forceinline__ void group_max(float (&v)[kVals], float* red, int par
 
 // --------------------------------------------------------------------------
 // quantize
+//
+// Signed map: each group stages its full blocks in shared memory one block
+// ahead.  While it works on block b, per-thread 16-byte cp.async copies bring
+// block b + stride into the group's other 8 KB buffer, and thread 0 asks L2
+// for block b + 2 stride.  Every thread copies and later reads the same
+// elements (its own slots), so its own cp.async.wait_group orders the two and
+// no barrier is needed; the wait is on the thread's own copies, which always
+// complete.  The signed code decision costs more instructions per value than
+// the unsigned one, and the copies in flight keep DRAM busy meanwhile.  The
+// unsigned map loads each block directly (its arithmetic is short enough that
+// staging did not pay).  Partial blocks and unaligned inputs are loaded
+// element-wise.
+
+constexpr int kQTabBytes = (kTablesBytes + 127) / 128 * 128;          // tables, then the stage
+constexpr int kQSmemBytes = kQTabBytes + kQGroups * 2 * BWD_BLOCK * 4;  // + 2 x 8 KB per group
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* src) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(src) : "memory");
+}
+
+// Block absmax, codes and stores of one full, aligned block whose 16 values
+// per thread are in v.
+template <bool kSigned>
+__device__ __forceinline__ void quantize_store_vec(const float (&v)[kPer], const bwd::Tables& tab, float* red,
+                                                   int parity, int group, int t, int64_t b,
+                                                   uint8_t* __restrict__ codes, float* __restrict__ absmax) {
+  float mx[1] = {0.0f};
+#pragma unroll
+  for (int j = 0; j < kPer; j += 2) mx[0] = max3abs(mx[0], v[j], v[j + 1]);
+  group_max<1>(mx, red, parity, group, t);
+  const float am = mx[0];
+  uint32_t w[kQuads];
+  quantize_quads<kSigned, true>(v, am, tab, w);
+#pragma unroll
+  for (int k = 0; k < kQuads; ++k)
+    __stcs(reinterpret_cast<unsigned int*>(codes + b * BWD_BLOCK + kSpan * k) + t, w[k]);
+  if (t == 0) absmax[b] = am;
+}
 
 template <bool kSigned>
 __global__ void __launch_bounds__(kQCta, 2)
@@ -305,7 +344,39 @@ quantize_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ co
   const int64_t nb = (n + BWD_BLOCK - 1) / BWD_BLOCK;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kQGroups;
   int it = 0;
-  for (int64_t b = static_cast<int64_t>(blockIdx.x) * kQGroups + group; b < nb; b += stride, ++it) {
+  int64_t b = static_cast<int64_t>(blockIdx.x) * kQGroups + group;
+  if (kSigned && vec_ok) {  // full blocks through the stage
+    const int64_t nfull = n / BWD_BLOCK;
+    float* stage = reinterpret_cast<float*>(smem_raw + kQTabBytes) + group * 2 * BWD_BLOCK;
+    if (b < nfull) {
+#pragma unroll
+      for (int k = 0; k < kQuads; ++k) cp_async16(stage + kSpan * k + 4 * t, x + b * BWD_BLOCK + kSpan * k + 4 * t);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    for (; b < nfull; b += stride, ++it) {
+      const int64_t bn = b + stride;
+      if (t == 0 && bn + stride < nfull) prefetch_l2(x + (bn + stride) * BWD_BLOCK, 8192u);
+      if (bn < nfull) {
+        float* nxt = stage + ((it + 1) & 1) * BWD_BLOCK;
+#pragma unroll
+        for (int k = 0; k < kQuads; ++k) cp_async16(nxt + kSpan * k + 4 * t, x + bn * BWD_BLOCK + kSpan * k + 4 * t);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      asm volatile("cp.async.wait_group 1;" ::: "memory");  // this block's copies (the older group)
+      const float* cur = stage + (it & 1) * BWD_BLOCK;
+      float v[kPer];
+#pragma unroll
+      for (int k = 0; k < kQuads; ++k) {
+        const float4 a = *reinterpret_cast<const float4*>(cur + kSpan * k + 4 * t);
+        v[4 * k] = a.x; v[4 * k + 1] = a.y; v[4 * k + 2] = a.z; v[4 * k + 3] = a.w;
+      }
+      quantize_store_vec<kSigned>(v, tab, s_red[group], it & 1, group, t, b, codes, absmax);
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  }
+  // direct loads (unsigned map; for the signed map only unaligned inputs and
+  // a partial last block remain)
+  for (; b < nb; b += stride, ++it) {
     const int64_t base = b * BWD_BLOCK;
     const int rem = static_cast<int>(rem_in_block(n, base));
     const bool vec = vec_ok && rem == BWD_BLOCK;
@@ -801,7 +872,7 @@ bwd_status ensure_device(DeviceState** out) {
       reinterpret_cast<const void*>(adam8bit_kernel<kF32, kF16>), reinterpret_cast<const void*>(adam8bit_kernel<kBF16, kF16>),
       reinterpret_cast<const void*>(adam8bit_kernel<kF16, kF16>)};
   for (int k = 0; k < 2; ++k) {
-    if ((s = occupancy(kq[k], kQCta, kTablesBytes, &d.occ_quant[k])) != BWD_OK) return s;
+    if ((s = occupancy(kq[k], kQCta, k == 0 ? kQSmemBytes : kTablesBytes, &d.occ_quant[k])) != BWD_OK) return s;
     if ((s = occupancy(kd[k], kDeqThreads, 0, &d.occ_dequant[k])) != BWD_OK) return s;
   }
   for (int k = 0; k < 9; ++k)
@@ -911,7 +982,7 @@ bwd_status bwd_quantize_blockwise(const float* x, int64_t n, bwd_map_kind kind, 
   const int vec = aligned16(x) && aligned16(codes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (kind == BWD_MAP_SIGNED)
-    quantize_kernel<true><<<grid_for(nb, kQGroups, *d, d->occ_quant[0]), kQCta, kTablesBytes, st>>>(
+    quantize_kernel<true><<<grid_for(nb, kQGroups, *d, d->occ_quant[0]), kQCta, kQSmemBytes, st>>>(
         x, n, codes, absmax, vec);
   else
     quantize_kernel<false><<<grid_for(nb, kQGroups, *d, d->occ_quant[1]), kQCta, kTablesBytes, st>>>(
