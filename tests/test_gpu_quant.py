@@ -138,6 +138,30 @@ def test_code_decision_sweep(bwd, signed):
     assert bad.size == 0, f"{bad.size} codes differ, first at value {rows[bad[0]]!r}"
 
 
+@pytest.mark.parametrize("offset", [0, 4])
+@pytest.mark.parametrize("signed", [True, False])
+def test_many_blocks_per_group_bit_exact(bwd, signed, offset):
+    """Enough blocks that every quantizer group and dequantizer CTA walks
+    several of them (the staged copies and the rotating output buffers are
+    reused), a partial last block, and buffers 16 bytes past the allocation
+    start (still the vector path): every code, absmax and value bit-exact."""
+    n = (1 << 24) + 5 * 2048 + 77
+    x = W.quant_input(n + offset, seed=21).to(DEV)
+    if not signed:
+        x = x * x
+    xv = x[offset:]
+    codes = torch.empty(n + offset, dtype=torch.uint8, device=DEV)[offset:]
+    absmax = torch.empty((n + 2047) // 2048, dtype=torch.float32, device=DEV)
+    bwd.quantize_blockwise(xv, kind(signed), codes=codes, absmax=absmax)
+    co, ao = oracle.quantize_blockwise(xv.cpu().numpy(), signed)
+    assert np.array_equal(absmax.cpu().numpy().view(U32), ao.view(U32))
+    assert np.array_equal(codes.cpu().numpy(), co)
+    out = torch.empty(n + offset, dtype=torch.float32, device=DEV)[offset:]
+    bwd.dequantize_blockwise(codes, absmax, kind(signed), out=out)
+    yo = oracle.dequantize_blockwise(co, ao, signed)
+    assert np.array_equal(out.cpu().numpy().view(U32), yo.view(U32))
+
+
 def test_full_size_2p28_sampled(bwd):
     """The 2^28-element workload: absmax of every block checked against a
     plain max, codes and dequantized values of sampled blocks bit-exact."""
