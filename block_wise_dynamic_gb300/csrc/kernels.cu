@@ -22,6 +22,9 @@
 // a warp reduction and a pass over the group's four warps through shared
 // memory, synchronised by a named barrier per group.  The maps and the
 // bucket entries (tables.h) are copied once per CTA into dynamic shared memory.
+// The signed standalone quantizer also stages each group's next block in
+// shared memory (cp.async); the dequantizer writes each block's output from
+// shared memory with one bulk copy.
 //
 // Exactness.  Every operation that decides a code is IEEE binary32 with
 // explicit round-to-nearest intrinsics (no contracted multiply-add): the
