@@ -72,11 +72,17 @@ def _stream_handle(device: torch.device, stream) -> int:
     return stream.cuda_stream
 
 
-def _need(t: torch.Tensor, name: str, dtype, numel: Optional[int] = None) -> None:
+def _need(t: torch.Tensor, name: str, dtype, numel: Optional[int] = None,
+          device: Optional[torch.device] = None) -> None:
+    """Type, layout and size checks; with ``device`` given, the tensor must
+    live on that device (the kernel is launched there, and a pointer into
+    another GPU's memory would fault)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call runs on {device}")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -115,8 +121,8 @@ def quantize_blockwise(x: torch.Tensor, kind="signed", codes=None, absmax=None, 
         codes = torch.empty(n, dtype=torch.uint8, device=x.device)
     if absmax is None:
         absmax = torch.empty(num_blocks(n), dtype=torch.float32, device=x.device)
-    _need(codes, "codes", torch.uint8, n)
-    _need(absmax, "absmax", torch.float32, num_blocks(n))
+    _need(codes, "codes", torch.uint8, n, x.device)
+    _need(absmax, "absmax", torch.float32, num_blocks(n), x.device)
     with torch.cuda.device(x.device):
         st = _lib.bwd_quantize_blockwise(
             x.data_ptr(), n, _kind(kind), codes.data_ptr(), absmax.data_ptr(), _stream_handle(x.device, stream)
@@ -129,10 +135,10 @@ def dequantize_blockwise(codes: torch.Tensor, absmax: torch.Tensor, kind="signed
     """map[code] * absmax[block] as a flat float32 tensor."""
     n = codes.numel()
     _need(codes, "codes", torch.uint8)
-    _need(absmax, "absmax", torch.float32, num_blocks(n))
+    _need(absmax, "absmax", torch.float32, num_blocks(n), codes.device)
     if out is None:
         out = torch.empty(n, dtype=torch.float32, device=codes.device)
-    _need(out, "out", torch.float32, n)
+    _need(out, "out", torch.float32, n, codes.device)
     with torch.cuda.device(codes.device):
         st = _lib.bwd_dequantize_blockwise(
             codes.data_ptr(), absmax.data_ptr(), n, _kind(kind), out.data_ptr(), _stream_handle(codes.device, stream)
@@ -172,11 +178,12 @@ def adam8bit_step(p, g, m_codes, m_absmax, v_codes, v_absmax, *, lr=1e-3, beta1=
     _need(p, "p", torch.float32)
     if g.dtype not in _GDT:
         raise TypeError("g must be float32, bfloat16 or float16")
-    _need(g, "g", g.dtype, n)
-    _need(m_codes, "m_codes", torch.uint8, n)
-    _need(v_codes, "v_codes", torch.uint8, n)
-    _need(m_absmax, "m_absmax", torch.float32, num_blocks(n))
-    _need(v_absmax, "v_absmax", torch.float32, num_blocks(n))
+    dev = p.device
+    _need(g, "g", g.dtype, n, dev)
+    _need(m_codes, "m_codes", torch.uint8, n, dev)
+    _need(v_codes, "v_codes", torch.uint8, n, dev)
+    _need(m_absmax, "m_absmax", torch.float32, num_blocks(n), dev)
+    _need(v_absmax, "v_absmax", torch.float32, num_blocks(n), dev)
     hp = _hparams(lr, beta1, beta2, eps, step, weight_decay)
     with torch.cuda.device(p.device):
         st = _lib.bwd_adam8bit_step(
@@ -203,16 +210,17 @@ class MultiTensorArgs:
         self.g_dtype = _GDT[gdt.pop()] if T else _abi.BWD_F32
         self.p_dtype = _GDT[pdt.pop()] if T else _abi.BWD_F32
         self.device = params[0].device if T else None
+        dev = self.device
         for i in range(T):
             n = params[i].numel()
-            _need(params[i], f"params[{i}]", params[i].dtype)
+            _need(params[i], f"params[{i}]", params[i].dtype, None, dev)
             if params[i].dtype not in _GDT:
                 raise TypeError("parameters must be float32, bfloat16 or float16")
-            _need(grads[i], f"grads[{i}]", grads[i].dtype, n)
-            _need(m_codes[i], f"m_codes[{i}]", torch.uint8, n)
-            _need(v_codes[i], f"v_codes[{i}]", torch.uint8, n)
-            _need(m_absmax[i], f"m_absmax[{i}]", torch.float32, num_blocks(n))
-            _need(v_absmax[i], f"v_absmax[{i}]", torch.float32, num_blocks(n))
+            _need(grads[i], f"grads[{i}]", grads[i].dtype, n, dev)
+            _need(m_codes[i], f"m_codes[{i}]", torch.uint8, n, dev)
+            _need(v_codes[i], f"v_codes[{i}]", torch.uint8, n, dev)
+            _need(m_absmax[i], f"m_absmax[{i}]", torch.float32, num_blocks(n), dev)
+            _need(v_absmax[i], f"v_absmax[{i}]", torch.float32, num_blocks(n), dev)
         arr = ctypes.c_void_p * T
         self.T = T
         self._keep = (list(params), list(grads), list(m_codes), list(m_absmax), list(v_codes), list(v_absmax))
@@ -222,8 +230,29 @@ class MultiTensorArgs:
         self.ma = arr(*[t.data_ptr() for t in m_absmax])
         self.vc = arr(*[t.data_ptr() for t in v_codes])
         self.va = arr(*[t.data_ptr() for t in v_absmax])
-        self.n = (ctypes.c_int64 * T)(*[t.numel() for t in params])
-        self.numel = int(sum(t.numel() for t in params))
+        self._sizes = [t.numel() for t in params]
+        self.n = (ctypes.c_int64 * T)(*self._sizes)
+        self.numel = int(sum(self._sizes))
+        self._gdtype = grads[0].dtype if T else None
+
+    def set_grads(self, grads: Sequence[torch.Tensor]) -> None:
+        """Points the table at new gradient tensors (same sizes, dtype and
+        device as before; non-contiguous ones are copied), leaving the
+        parameter and state pointers as they are.  This is the per-step work
+        when gradients are fresh tensors every step."""
+        if len(grads) != self.T:
+            raise ValueError(f"expected {self.T} gradients, got {len(grads)}")
+        dev, gdt = self.device, self._gdtype
+        if not all(isinstance(g, torch.Tensor) and g.dtype == gdt for g in grads):
+            raise TypeError(f"every gradient must be a {gdt} tensor, as when the table was built")
+        if [g.numel() for g in grads] != self._sizes:
+            raise ValueError("gradient sizes differ from the parameters'")
+        if not all(g.device == dev for g in grads):
+            raise ValueError(f"every gradient must be on {dev}")
+        if not all(g.is_contiguous() for g in grads):
+            grads = [g if g.is_contiguous() else g.contiguous() for g in grads]
+        self._keep = (self._keep[0], list(grads)) + self._keep[2:]
+        self.g[:] = [g.data_ptr() for g in grads]
 
     def step(self, *, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step,
              stream=None) -> None:

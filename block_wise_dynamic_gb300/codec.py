@@ -48,7 +48,7 @@ def load_from_fp32_adam(opt8, fp32_opt: torch.optim.Optimizer) -> None:
         step = st.get("step", 0)
         step = int(step.item()) if torch.is_tensor(step) else int(step)
         opt8.state[p] = {"step": step, "m_codes": mc, "m_absmax": ma, "v_codes": vc, "v_absmax": va}
-    opt8._args_cache = {}
+    opt8._reset_plans()
 
 
 def export_fp32_adam_state(opt8) -> Dict[torch.Tensor, dict]:

@@ -392,10 +392,13 @@ embed_bwd_staged_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, con
   __syncthreads();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kSGroups;
   const int64_t tok0 = static_cast<int64_t>(blockIdx.x) * kSGroups + group;
-  // copies of token `tok` into buffer `b` (nothing for an id outside [0, V))
+  // copies of token `tok` into buffer `b` (nothing for an id outside [0, V));
+  // thread 0 counts the phases it started per buffer (for the drain below)
+  uint32_t issued[2] = {0u, 0u};
   auto issue = [&](int64_t tok, int b) {
     const int64_t id = ids[tok];
     if (id < 0 || id >= vocab) return;
+    ++issued[b];
     uint64_t* bar = &s_full[group][b];
     mbar_expect_tx(bar, 2u * row_bytes);
     bulk_g2s(gbuf + b * 2 * dim, w + id * static_cast<int64_t>(dim), row_bytes, bar);
@@ -407,11 +410,6 @@ embed_bwd_staged_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, con
   for (int k = 0; k < kSChunks; ++k) pg[k] = pb[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   uint32_t phase = 0;  // bit b: parity of buffer b's next phase
   int slot = 0;
-  int pending = -1;    // buffer with copies issued and not yet waited for
-  if (tok0 < num_tokens) {
-    const int64_t id0 = ids[tok0];
-    if (id0 >= 0 && id0 < vocab) pending = 0;
-  }
   int it = 0;
   for (int64_t tok = tok0; tok < num_tokens; tok += stride, ++it) {
     const int b = it & 1;
@@ -425,14 +423,6 @@ embed_bwd_staged_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, con
     if (!ok) {
       atomicOr(&g_embed_fault, 1u);
       s_abort[group][(it + 1) & 1] = 1;
-    }
-    {
-      const int64_t nx = tok + stride;
-      pending = -1;
-      if (nx < num_tokens) {
-        const int64_t nid = ids[nx];
-        if (nid >= 0 && nid < vocab) pending = b ^ 1;
-      }
     }
     const float mu = mean[tok], r = rstd[tok];
     const float* xs = gbuf + b * 2 * dim;
@@ -483,9 +473,15 @@ embed_bwd_staged_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, con
       }
     }
   }
-  // a group that gave up lets its copy in flight land (bounded) before the
-  // buffers are reused below
-  if (t == 0 && pending >= 0 && (s_abort[group][0] || s_abort[group][1])) mbar_wait(&s_full[group][pending], (phase >> pending) & 1u);
+  // A group that gave up lets every copy it started land (bounded) before
+  // the buffers are reused below: the one whose wait timed out and the one
+  // issued ahead.  The k-th copy into a buffer completes its phase k - 1;
+  // waiting on the parity of a phase that already completed returns at once.
+  if (t == 0 && (s_abort[group][0] || s_abort[group][1])) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+      if (issued[b] > 0) mbar_wait(&s_full[group][b], (issued[b] - 1u) & 1u);
+  }
   __syncthreads();
   // partials: each group's into its first buffer, then summed over the groups in order
   float* const part = s_buf + static_cast<int64_t>(group) * 4 * dim;
@@ -525,6 +521,7 @@ __global__ void __launch_bounds__(32) bounded_wait_selftest_kernel() {
 
 struct EmbedDevice {
   bool ready = false;
+  unsigned long long ctx = 0;  // context the kernel attributes were set in
   int num_sms = 0;
   int occ_fwd = 1;
   int occ_slow_fwd = 1;
@@ -539,9 +536,13 @@ bwd_status ensure_device(EmbedDevice** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(BWD_ERR_CUDA, "device ordinal %d unsupported", dev);
+  unsigned long long ctx = 0;
+  bwd_status s = bwd::host::current_context_id(&ctx);
+  if (s != BWD_OK) return s;
   std::lock_guard<std::mutex> lock(g_mu);
   EmbedDevice& d = g_dev[dev];
-  if (!d.ready) {
+  if (!d.ready || d.ctx != ctx) {
+    d.ready = false;
     if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute");
     if ((e = cudaFuncSetAttribute(reinterpret_cast<const void*>(embed_bwd_staged_kernel),
@@ -558,6 +559,7 @@ bwd_status ensure_device(EmbedDevice** out) {
         return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
       *o.out = v > 0 ? v : 1;
     }
+    d.ctx = ctx;
     d.ready = true;
   }
   *out = &d;

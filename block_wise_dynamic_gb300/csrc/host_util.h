@@ -23,6 +23,14 @@ bwd_status check_launch(const char* what);
 // This thread's last error message ("" if none).
 const char* last_error();
 
+// Unique id of the current CUDA context (the driver's cuCtxGetId, unique for
+// the life of the process).  Per-device state cached by the library (the
+// uploaded code tables, kernel attributes) belongs to one context: after a
+// cudaDeviceReset or a released primary context the id changes and the state
+// is set up again.  Initialises the device's primary context if none is
+// current.
+bwd_status current_context_id(unsigned long long* id);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // p is a multiple of `bytes` (a power of two): element pointers must be

@@ -805,6 +805,31 @@ bwd_status check_launch(const char* what) {
 
 const char* last_error() { return t_last_error.c_str(); }
 
+namespace {
+using CtxGetIdFn = int (*)(void* ctx, unsigned long long* id);  // CUresult cuCtxGetId(CUcontext, ...)
+std::once_flag g_ctx_fn_once;
+CtxGetIdFn g_ctx_fn = nullptr;
+}  // namespace
+
+bwd_status current_context_id(unsigned long long* id) {
+  std::call_once(g_ctx_fn_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_fn = reinterpret_cast<CtxGetIdFn>(fn);
+  });
+  if (!g_ctx_fn) return fail(BWD_ERR_CUDA, "the driver does not provide cuCtxGetId");
+  if (g_ctx_fn(nullptr, id) == 0) return BWD_OK;
+  // no current context yet: make the current device's primary context current
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  if (g_ctx_fn(nullptr, id) != 0) return fail(BWD_ERR_CUDA, "cuCtxGetId failed for the current context");
+  return BWD_OK;
+}
+
 }  // namespace host
 }  // namespace bwd
 
@@ -818,6 +843,7 @@ using bwd::host::fail;
 
 struct DeviceState {
   bool ready = false;
+  unsigned long long ctx = 0;  // context the tables were uploaded to
   int num_sms = 0;
   int occ_quant[2] = {0, 0};
   int occ_dequant[2] = {0, 0};
@@ -850,9 +876,13 @@ bwd_status ensure_device(DeviceState** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(BWD_ERR_CUDA, "device ordinal %d unsupported", dev);
+  unsigned long long ctx = 0;
+  bwd_status s = bwd::host::current_context_id(&ctx);
+  if (s != BWD_OK) return s;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& d = g_dev[dev];
-  if (d.ready) { *out = &d; return BWD_OK; }
+  if (d.ready && d.ctx == ctx) { *out = &d; return BWD_OK; }
+  d.ready = false;  // first use, or a new context (its __device__ tables start zeroed)
   if (!g_host_built) {
     char err[128] = {0};
     if (bwd::build_tables(&g_host_tables, err, sizeof err) != 0)
@@ -863,7 +893,6 @@ bwd_status ensure_device(DeviceState** out) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol(tables)");
   e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  bwd_status s;
   const void* kq[2] = {reinterpret_cast<const void*>(quantize_kernel<true>),
                        reinterpret_cast<const void*>(quantize_kernel<false>)};
   const void* kd[2] = {reinterpret_cast<const void*>(dequantize_kernel<true>),
@@ -880,6 +909,7 @@ bwd_status ensure_device(DeviceState** out) {
   }
   for (int k = 0; k < 9; ++k)
     if ((s = occupancy(ka[k], kCta, kTablesBytes, &d.occ_adam[k])) != BWD_OK) return s;
+  d.ctx = ctx;
   d.ready = true;
   *out = &d;
   return BWD_OK;

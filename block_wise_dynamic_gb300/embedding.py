@@ -36,8 +36,8 @@ def xavier_bound(num_embeddings: int, dim: int) -> float:
     return b
 
 
-def _ids(ids: torch.Tensor) -> torch.Tensor:
-    _need(ids, "ids", torch.int64)
+def _ids(ids: torch.Tensor, device: torch.device) -> torch.Tensor:
+    _need(ids, "ids", torch.int64, None, device)
     return ids
 
 
@@ -54,7 +54,7 @@ def init_weight(weight: torch.Tensor, words: torch.Tensor | None = None, generat
                               generator=generator).to(torch.int32)
     if words.dtype not in (torch.int32, torch.uint32):
         raise TypeError("words must be int32 or uint32")
-    _need(words, "words", words.dtype, n)
+    _need(words, "words", words.dtype, n, weight.device)
     with torch.cuda.device(weight.device):
         st = _lib.bwd_embedding_init(words.data_ptr(), weight.shape[0], weight.shape[1], weight.data_ptr(),
                                      _stream_handle(weight.device, stream))
@@ -66,13 +66,14 @@ def forward(ids: torch.Tensor, weight: torch.Tensor, gamma: torch.Tensor, beta: 
             need_stats: bool = True, stream=None):
     """y (ids.shape + (D,)), and per-token mean and rstd (None when
     ``need_stats`` is false)."""
-    _ids(ids)
     if weight.dim() != 2:
         raise ValueError("weight must be (num_embeddings, dim)")
     v, d = weight.shape
     _need(weight, "weight", torch.float32)
-    _need(gamma, "gamma", torch.float32, d)
-    _need(beta, "beta", torch.float32, d)
+    dev = weight.device
+    _ids(ids, dev)
+    _need(gamma, "gamma", torch.float32, d, dev)
+    _need(beta, "beta", torch.float32, d, dev)
     t = ids.numel()
     y = torch.empty(*ids.shape, d, dtype=torch.float32, device=weight.device)
     mean = torch.empty(t, dtype=torch.float32, device=weight.device) if need_stats else None
@@ -89,17 +90,20 @@ def forward(ids: torch.Tensor, weight: torch.Tensor, gamma: torch.Tensor, beta: 
 def backward(ids: torch.Tensor, weight: torch.Tensor, gamma: torch.Tensor, mean: torch.Tensor, rstd: torch.Tensor,
              dy: torch.Tensor, dweight: torch.Tensor, dgamma: torch.Tensor, dbeta: torch.Tensor, stream=None) -> None:
     """Accumulates the gradients into dweight (V, D), dgamma and dbeta (D)."""
-    _ids(ids)
+    if weight.dim() != 2:
+        raise ValueError("weight must be (num_embeddings, dim)")
     v, d = weight.shape
     t = ids.numel()
     _need(weight, "weight", torch.float32)
-    _need(gamma, "gamma", torch.float32, d)
-    _need(mean, "mean", torch.float32, t)
-    _need(rstd, "rstd", torch.float32, t)
-    _need(dy, "dy", torch.float32, t * d)
-    _need(dweight, "dweight", torch.float32, v * d)
-    _need(dgamma, "dgamma", torch.float32, d)
-    _need(dbeta, "dbeta", torch.float32, d)
+    dev = weight.device
+    _ids(ids, dev)
+    _need(gamma, "gamma", torch.float32, d, dev)
+    _need(mean, "mean", torch.float32, t, dev)
+    _need(rstd, "rstd", torch.float32, t, dev)
+    _need(dy, "dy", torch.float32, t * d, dev)
+    _need(dweight, "dweight", torch.float32, v * d, dev)
+    _need(dgamma, "dgamma", torch.float32, d, dev)
+    _need(dbeta, "dbeta", torch.float32, d, dev)
     with torch.cuda.device(weight.device):
         st = _lib.bwd_embedding_backward(
             ids.data_ptr(), t, weight.data_ptr(), v, d, gamma.data_ptr(), mean.data_ptr(), rstd.data_ptr(),

@@ -14,7 +14,10 @@ the update, stored back rounded to nearest even); gradients fp32, bf16 or
 fp16.  Per parameter the state holds ``step`` and the codes and absmax of
 both moments; ``state_dict()`` / ``load_state_dict()`` round-trip them
 exactly.  Each ``step()`` issues one multi-tensor launch per (device,
-gradient dtype, step count) group.
+gradient dtype, step count) group.  The launch tables are built once per
+parameter group and reused: when gradients are fresh tensors each step (the
+default ``zero_grad(set_to_none=True)``), a step only re-reads the gradient
+pointers.
 """
 
 from __future__ import annotations
@@ -52,6 +55,34 @@ class Adam8bit(torch.optim.Optimizer):
             st["m_codes"], st["m_absmax"], st["v_codes"], st["v_absmax"] = mc, ma, vc, va
         return st
 
+    def _plan(self, params, grads):
+        """Launch plan of one parameter group: its parameters with a gradient,
+        bucketed by (device, parameter dtype, gradient dtype, step count), each
+        bucket with its argument table (parameter and state pointers fixed)."""
+        buckets = defaultdict(list)
+        for i, (p, g) in enumerate(zip(params, grads)):
+            if g is None:
+                continue
+            if p.dtype not in (torch.float32, torch.bfloat16, torch.float16) or not p.is_cuda:
+                raise TypeError("Adam8bit needs fp32, bf16 or fp16 CUDA parameters")
+            if g.is_sparse:
+                raise TypeError("sparse gradients are not supported")
+            st = self._state_for(p)
+            if st["m_absmax"].numel() != num_blocks(p.numel()):
+                raise ValueError("state does not match the parameter size")
+            buckets[(p.device, p.dtype, g.dtype, st["step"])].append(i)
+        plan = []
+        for (_, _, _, t), idx in buckets.items():
+            sts = [self.state[params[i]] for i in idx]
+            gs = [grads[i] if grads[i].is_contiguous() else grads[i].contiguous() for i in idx]
+            args = MultiTensorArgs(
+                [params[i].view(-1) for i in idx], [g.view(-1) for g in gs],
+                [s["m_codes"] for s in sts], [s["m_absmax"] for s in sts],
+                [s["v_codes"] for s in sts], [s["v_absmax"] for s in sts],
+            )
+            plan.append([idx, sts, args, t])
+        return {"params": list(params), "has_grad": [g is not None for g in grads], "buckets": plan}
+
     @torch.no_grad()
     def step(self, closure=None):
         loss = None
@@ -59,41 +90,38 @@ class Adam8bit(torch.optim.Optimizer):
             with torch.enable_grad():
                 loss = closure()
         for gi, group in enumerate(self.param_groups):
-            buckets = defaultdict(list)
-            for p in group["params"]:
-                if p.grad is None:
-                    continue
-                if p.dtype not in (torch.float32, torch.bfloat16, torch.float16) or not p.is_cuda:
-                    raise TypeError("Adam8bit needs fp32, bf16 or fp16 CUDA parameters")
-                if p.grad.is_sparse:
-                    raise TypeError("sparse gradients are not supported")
-                st = self._state_for(p)
-                if st["m_absmax"].numel() != num_blocks(p.numel()):
-                    raise ValueError("state does not match the parameter size")
-                st["step"] += 1
-                buckets[(p.device, p.dtype, p.grad.dtype, st["step"])].append(p)
+            params = group["params"]
+            grads = [p.grad for p in params]
+            plan = self._args_cache.get(gi)
+            fresh = (plan is None or len(plan["params"]) != len(params)
+                     or not all(a is b for a, b in zip(plan["params"], params))
+                     or plan["has_grad"] != [g is not None for g in grads])
+            if fresh:
+                plan = self._args_cache[gi] = self._plan(params, grads)
             b1, b2 = group["betas"]
-            for (dev, pdt, gdt, t), ps in buckets.items():
-                grads = [q.grad if q.grad.is_contiguous() else q.grad.contiguous() for q in ps]
-                sts = [self.state[q] for q in ps]
-                key = (gi, dev, pdt, gdt)
-                ptrs = tuple(x.data_ptr() for x in ps) + tuple(x.data_ptr() for x in grads)
-                cached = self._args_cache.get(key)
-                if cached is None or cached[0] != ptrs:
-                    args = MultiTensorArgs(
-                        [q.view(-1) for q in ps], [x.view(-1) for x in grads],
-                        [s["m_codes"] for s in sts], [s["m_absmax"] for s in sts],
-                        [s["v_codes"] for s in sts], [s["v_absmax"] for s in sts],
-                    )
-                    self._args_cache[key] = (ptrs, args)
-                else:
-                    args = cached[1]
+            for bucket in plan["buckets"]:
+                idx, sts, args, t = bucket
+                if not fresh:
+                    try:
+                        args.set_grads([grads[i] for i in idx])
+                    except (TypeError, ValueError):
+                        # a gradient changed dtype or shape: rebuild this group's plan next step
+                        self._args_cache.pop(gi, None)
+                        raise
                 args.step(lr=group["lr"], beta1=b1, beta2=b2, eps=group["eps"],
-                          weight_decay=group["weight_decay"], step=t)
+                          weight_decay=group["weight_decay"], step=t + 1)
+                # the step count advances only once its launch went through
+                bucket[3] = t + 1
+                for s in sts:
+                    s["step"] = t + 1
         return loss
 
-    def load_state_dict(self, state_dict):
+    def _reset_plans(self):
+        """Forget the cached launch plans (after the state was replaced)."""
         self._args_cache = {}
+
+    def load_state_dict(self, state_dict):
+        self._reset_plans()
         super().load_state_dict(state_dict)
         # torch casts every floating parameter's state tensors to the
         # parameter dtype; codes are integers 0..255, so casting back is exact

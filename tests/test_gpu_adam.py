@@ -311,6 +311,42 @@ def test_adamw8bit_optimizer_matches_oracle(bwd):
         compare_step(got, r)
 
 
+def test_optimizer_skipped_gradients_and_failed_step(bwd):
+    """The drop-in optimizer with fresh gradient tensors every step: a
+    parameter without a gradient is skipped (its step count stays), the
+    launch plan is rebuilt when that pattern changes, and a step whose launch
+    is refused leaves every step count where it was."""
+    torch.manual_seed(2)
+    sizes = (5000, 2048 * 2, 17)
+    ps = [torch.nn.Parameter(torch.randn(n, device=DEV) * 0.02) for n in sizes]
+    ref = [[p.detach().cpu().numpy().copy(), *oracle.state_init(p.numel())] for p in ps]
+    steps = [0, 0, 0]
+    opt = bwd.Adam8bit(ps, lr=1e-3)
+    pattern = [(0, 1, 2), (0, 2), (0, 2), (0, 1, 2), (0, 1, 2)]
+    for k, live in enumerate(pattern):
+        for i, p in enumerate(ps):
+            p.grad = torch.randn(p.numel(), device=DEV) * 1e-2 if i in live else None
+        if k == 3:  # a refused launch (non-finite lr): nothing moves
+            opt.param_groups[0]["lr"] = float("nan")
+            before = [p.detach().clone() for p in ps]
+            with pytest.raises(bwd.BwdError):
+                opt.step()
+            assert [opt.state[p]["step"] for p in ps] == steps
+            assert all(torch.equal(a, b.detach()) for a, b in zip(before, ps))
+            opt.param_groups[0]["lr"] = 1e-3
+        opt.step()
+        for i in live:
+            steps[i] += 1
+            hp = oracle.AdamHParams(lr=1e-3, step=steps[i])
+            ref[i] = list(oracle.adam8bit_step(ref[i][0], ps[i].grad.cpu().numpy(), *ref[i][1:], hp))
+        assert [opt.state[p]["step"] for p in ps] == steps
+    for p, r in zip(ps, ref):
+        st = opt.state[p]
+        got = (p.detach().cpu().numpy(), st["m_codes"].cpu().numpy(), st["m_absmax"].cpu().numpy(),
+               st["v_codes"].cpu().numpy(), st["v_absmax"].cpu().numpy())
+        compare_step(got, tuple(r))
+
+
 def test_step_on_tensor_larger_than_2p31_elements(bwd):
     """64-bit indexing in the fused step: one tensor of 2^31 + 5 parameters;
     blocks at the 2^31 boundary and the ragged tail against the oracle."""
