@@ -57,6 +57,8 @@ def parse_args():
                     help="parameter storage (bf16: widened for the update, rounded back)")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the other configurations and the optimizer host-path leg (N=1 only)")
     return ap.parse_args()
 
 
@@ -257,6 +259,13 @@ def _oracle_step_fn(kind: str, n: int, seed: int):
     return step
 
 
+def _spread(rates):
+    """min, max and coefficient of variation of per-process rates."""
+    m = statistics.fmean(rates)
+    cv = statistics.pstdev(rates) / m if len(rates) > 1 and m > 0 else 0.0
+    return {"per_process_min": min(rates), "per_process_max": max(rates), "per_process_cv": cv}
+
+
 def _pool_worker(kind, n, steps, warm, seed, barrier, out):
     import torch
 
@@ -303,6 +312,7 @@ def oracle_pool_rate(kind: str, n: int, steps: int, warm: int = 1, procs: int | 
                 w.terminate()
     dt = max(dts)
     per = 4 if kind == "quant" else 1
+    oracle_pool_rate.last_spread = _spread([per * n * steps / x for x in dts])
     return per * n * steps * procs / dt, dt, procs
 
 
@@ -311,10 +321,11 @@ def cpu_baseline_leg():
     rate, dt, procs = oracle_pool_rate("adam", n, steps=2, warm=0)
     one, dt1 = oracle_rate(n, steps=1, warm=0)
     return {"value": rate, "unit": "params/s", "cores": procs, "kind": "oracle",
-            "single_core_value": one,
+            "single_core_value": one, **oracle_pool_rate.last_spread,
             "sample": f"2 steps of the oracle in each of {procs} processes, each on its own {n} params "
                       f"(2048 blocks) of the same distributions, {dt:.1f} s for the slowest; one process "
-                      f"alone: {one:.3g} params/s"}
+                      f"alone: {one:.3g} params/s; value = all processes' params / the slowest process's "
+                      f"time, per-process rates beside it"}
 
 
 def run_reference(args):
@@ -466,6 +477,14 @@ def run_ours(args):
                        "untimed step"}
         del gh, ph, ghv, phv, pipe
 
+    secondary = optimizer = None
+    if world == 1 and not args.no_secondary and args.workload == "llama2_7b" and args.param_dtype == "f32":
+        del ps, gs, sts, mt
+        torch.cuda.empty_cache()
+        secondary = secondary_legs(dev)
+        optimizer = {name: time_optimizer_host_path(name, dev, steps=6, warmup=2)
+                     for name in ("llama2_7b", "ragged_2000")}
+
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -517,11 +536,194 @@ def run_ours(args):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if secondary is not None:
+        line["secondary"] = secondary
+    if optimizer is not None:
+        line["optimizer_host_path"] = optimizer
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_leg()
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# other configurations and the drop-in optimizer, measured in the same run
+
+
+def _adam_tensors(wl, pdtype, dev, seed_base=0, grad_dtype=None):
+    import torch
+
+    import block_wise_dynamic_gb300 as bwd
+    from block_wise_dynamic_gb300 import workloads as W
+
+    sizes = [n for n in wl.sizes if n > 0]
+    gdt = grad_dtype or wl.grad_dtype
+    ps, gs, sts = [], [], []
+    for i, n in enumerate(sizes):
+        ps.append(W.gen_normal(n, 0.02, seed=seed_base + i, device=dev, dtype=pdtype))
+        gs.append(W.gen_normal(n, wl.grad_std[i], seed=seed_base + 500_000 + i, device=dev, dtype=gdt))
+        sts.append(bwd.state_init(n, dev))
+    return sizes, ps, gs, sts
+
+
+def time_adam_workload(name: str, param_dtype: str, dev, steps: int, warmup: int) -> dict:
+    """One multi-tensor step per timed iteration over a whole workload (as
+    the headline line, fewer steps); CUDA events on the launching stream.
+    Sets smaller than L2 are timed after an L2 flush per step."""
+    import torch
+
+    import block_wise_dynamic_gb300 as bwd
+    from block_wise_dynamic_gb300 import workloads as W
+
+    wl = W.workload(name)
+    pdtype = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[param_dtype]
+    sizes, ps, gs, sts = _adam_tensors(wl, pdtype, dev)
+    mt = bwd.MultiTensorArgs(ps, gs, *[[s[k] for s in sts] for k in range(4)])
+    N = sum(sizes)
+    gbytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
+    bpp = algorithmic_bytes_per_param(gbytes, 4 if pdtype == torch.float32 else 2)
+    flush = bpp * N < 2 * L2_BYTES
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    stream = torch.cuda.current_stream(dev)
+    hp = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps)
+    t = 0
+    for _ in range(warmup):
+        t += 1
+        mt.step(step=t, **hp)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for a, b in ev:
+        if flush:
+            scrub.fill_(1.0)
+        t += 1
+        a.record(stream)
+        mt.step(step=t, **hp)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+    peak, _ = measured_peak()
+    gbs = bpp * N / (ms / 1e3) / 1e9
+    out = {"workload": name, "param_dtype": param_dtype, "grad_dtype": "bf16" if gbytes == 2 else "f32",
+           "tensors": len(sizes), "params": N, "launches_per_step": math.ceil(len(sizes) / 448),
+           "steps": steps, "warmup": warmup, "ms_per_step": ms, "params_per_s": N / (ms / 1e3),
+           "bytes_per_param": bpp, "gbs": gbs, "frac": gbs / peak,
+           "l2": "flushed before each step (set smaller than L2)" if flush else "set larger than L2, no flush"}
+    del mt, ps, gs, sts, scrub
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_quant_passes(dev, steps: int, warmup: int) -> dict:
+    """The four standalone passes of quant_2p28 (2^28 fp32 elements)."""
+    import torch
+
+    import block_wise_dynamic_gb300 as bwd
+    from block_wise_dynamic_gb300 import workloads as W
+
+    n = 1 << 28
+    x = W.quant_input(n, seed=0, device=dev)
+    x2 = x * x
+    codes = torch.empty(n, dtype=torch.uint8, device=dev)
+    absmax = torch.empty(bwd.num_blocks(n), dtype=torch.float32, device=dev)
+    y = torch.empty(n, dtype=torch.float32, device=dev)
+    passes = [
+        ("quantize_signed", lambda: bwd.quantize_blockwise(x, "signed", codes, absmax)),
+        ("dequantize_signed", lambda: bwd.dequantize_blockwise(codes, absmax, "signed", out=y)),
+        ("quantize_unsigned", lambda: bwd.quantize_blockwise(x2, "unsigned", codes, absmax)),
+        ("dequantize_unsigned", lambda: bwd.dequantize_blockwise(codes, absmax, "unsigned", out=y)),
+    ]
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        for _, f in passes:
+            f()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in passes]
+          for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for k in range(steps):
+        for j, (_, f) in enumerate(passes):
+            ev[k][j][0].record(stream)
+            f()
+            ev[k][j][1].record(stream)
+    torch.cuda.synchronize(dev)
+    peak, _ = measured_peak()
+    out = {"workload": "quant_2p28", "elements": n, "steps": steps, "warmup": warmup,
+           "bytes_per_elem": QUANT_BYTES_PER_ELEM, "l2": "1 GiB fp32 per pass vs L2, no flush"}
+    for j, (name, _) in enumerate(passes):
+        ms = statistics.fmean(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(steps))
+        gbs = QUANT_BYTES_PER_ELEM * n / (ms / 1e3) / 1e9
+        out[name] = {"ms": ms, "elems_per_s": n / (ms / 1e3), "gbs": gbs, "frac": gbs / peak}
+    del x, x2, codes, absmax, y
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_optimizer_host_path(name: str, dev, steps: int, warmup: int) -> dict:
+    """The drop-in path a user calls, Adam8bit.step(), with fresh gradient
+    tensors every step (two alternating sets of fp32 gradients, so the
+    pointers change each step as under zero_grad(set_to_none=True)).
+    host_ms: wall time of opt.step() on the host (Python, argument
+    marshalling, launches; no synchronisation).  step_ms: CUDA events
+    around it.  kernel_ms: the same tensors through a prebuilt
+    MultiTensorArgs."""
+    import torch
+
+    import block_wise_dynamic_gb300 as bwd
+    from block_wise_dynamic_gb300 import workloads as W
+
+    wl = W.workload(name)
+    sizes = [n for n in wl.sizes if n > 0]
+    params = [torch.nn.Parameter(W.gen_normal(n, 0.02, seed=i, device=dev)) for i, n in enumerate(sizes)]
+    gsets = [[W.gen_normal(n, wl.grad_std[i], seed=1_000_000 * (k + 1) + i, device=dev) for i, n in enumerate(sizes)]
+             for k in range(2)]
+    opt = bwd.Adam8bit(params, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps)
+    stream = torch.cuda.current_stream(dev)
+    host, ev = [], []
+    for k in range(warmup + steps):
+        for p, g in zip(params, gsets[k % 2]):
+            p.grad = g
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        h0 = time.perf_counter()
+        opt.step()
+        h1 = time.perf_counter()
+        b.record(stream)
+        if k >= warmup:
+            host.append(1e3 * (h1 - h0))
+            ev.append((a, b))
+    torch.cuda.synchronize(dev)
+    step_ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+    st = [opt.state[p] for p in params]
+    mt = bwd.MultiTensorArgs([p.view(-1) for p in params], gsets[0],
+                             *[[s[k] for s in st] for k in ("m_codes", "m_absmax", "v_codes", "v_absmax")])
+    t = st[0]["step"]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+    torch.cuda.synchronize(dev)
+    for a, b in kev:
+        t += 1
+        a.record(stream)
+        mt.step(lr=wl.lr, step=t)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    kernel_ms = statistics.fmean(a.elapsed_time(b) for a, b in kev)
+    host_ms = statistics.fmean(host)
+    out = {"workload": name, "tensors": len(sizes), "params": sum(sizes), "grad_dtype": "f32",
+           "steps": steps, "warmup": warmup, "host_ms_per_step": host_ms,
+           "host_ms_max": max(host), "step_ms": step_ms, "kernel_ms": kernel_ms,
+           "host_below_kernel": host_ms < kernel_ms}
+    del opt, params, gsets, mt, st
+    torch.cuda.empty_cache()
+    return out
+
+
+def secondary_legs(dev, steps: int = 8, warmup: int = 3) -> dict:
+    """Every other configuration of the path, timed on this GPU in this run."""
+    legs = {}
+    for name, pdt in (("ragged_2000", "f32"), ("gpt_350m", "f32"), ("adam_1m", "f32"),
+                      ("llama2_7b", "bf16"), ("llama2_7b", "f16")):
+        legs[f"{name}/p_{pdt}"] = time_adam_workload(name, pdt, dev, steps, warmup)
+    legs["quant_2p28"] = time_quant_passes(dev, steps, warmup)
+    return legs
 
 
 QUANT_BYTES_PER_ELEM = 4 + 1 + 4.0 / 2048  # fp32 in or out, one code, absmax per block

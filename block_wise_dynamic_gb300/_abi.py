@@ -65,6 +65,7 @@ _SIGNATURES = {
         _int,
         [_i32, _pp, _int, _pp, _int, _pp, _pp, _pp, _pp, ctypes.POINTER(_i64), ctypes.POINTER(AdamHParams), _vp],
     ),
+    "bwd_zero_shard": (_int, [_i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "bwd_embedding_init": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "bwd_embedding_xavier_bound": (ctypes.c_float, [_i64, _i64]),
     "bwd_embedding_forward": (

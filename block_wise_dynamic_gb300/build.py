@@ -1,7 +1,7 @@
 """Builds the C-ABI shared library ``libbwd.so`` in-tree for sm_103a.
 
-Three translation units (the host codebook builder, the optimizer kernels and
-the stable-embedding kernels) are compiled in parallel and linked with the
+Four translation units (the host codebook builder, the host shard planner,
+the optimizer kernels and the stable-embedding kernels) are compiled in parallel and linked with the
 static CUDA runtime, so the library depends only on the driver.  No
 fast-math: every code decision must be IEEE.
 """
@@ -26,6 +26,7 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-
 
 SOURCES = {
     "codebook.o": os.path.join(CSRC, "codebook.cpp"),
+    "shard.o": os.path.join(CSRC, "shard.cpp"),
     "kernels.o": os.path.join(CSRC, "kernels.cu"),
     "embedding.o": os.path.join(CSRC, "embedding.cu"),
 }
@@ -61,7 +62,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
             if verbose:
                 cmd.insert(1, "-Xptxas=-v")
         else:
-            cmd = ["g++", *HOST_FLAGS, "-I", INCLUDE, "-c", src, "-o", out]
+            cuda_inc = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "include")
+            cmd = ["g++", *HOST_FLAGS, "-I", INCLUDE, "-I", cuda_inc, "-c", src, "-o", out]
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
     for cmd, pr in procs:
         log, _ = pr.communicate()

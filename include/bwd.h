@@ -173,6 +173,38 @@ bwd_status bwd_adam8bit_step_multi_ex(int32_t num_tensors, void* const* p,
                                       const bwd_adam_hparams* hp, void* stream);
 
 /* ------------------------------------------------------------------------
+ * ZeRO-style sharding of the step over P processes ("Яндекс Публикует ЯЛМ
+ * 100Б", section "ZeRO" under "Случай с несколькими графическими
+ * процессорами": each process keeps the values and optimizer state of its own
+ * group of parameters and alone updates them, so its step is O(N / P); the
+ * gradients are reduced before the step and the parameters gathered after
+ * it).  Blocks are independent (section 二 / 逐块量化 of the 8-bit optimizer
+ * page), so the split follows block boundaries and a rank's step over its
+ * pieces (bwd_adam8bit_step_multi / _ex, pointers offset by `offset`
+ * elements) equals the unsharded step on those elements bit for bit.
+ *
+ * Layout: in a padded flat space tensor i occupies the blocks
+ * [B_i, B_i + ceil(n_i / 2048)), B the prefix sums of the block counts and NB
+ * their total; rank r owns the K = ceil(NB / world) blocks [r K, (r + 1) K)
+ * clipped to NB (the last ranks may own fewer, or none), so padded buffers of
+ * world * K * 2048 elements split into equal per-rank slices.
+ *   n               : HOST int64[num_tensors], tensor sizes (0 allowed).
+ *   world, rank     : 1 <= world, 0 <= rank < world.
+ *   blocks_per_rank : HOST int64 out, K (may be NULL).
+ *   num_pieces      : HOST int32 out, the tensors the rank's blocks touch.
+ *   tensor, offset, count : HOST arrays of capacity num_tensors, written
+ *            (each may be NULL): piece j is the elements
+ *            [offset[j], offset[j] + count[j]) of tensor tensor[j]; offsets
+ *            are multiples of 2048; pieces ascend in tensor order.
+ * Host only (no device is touched).  BWD_ERR_INVALID_ARG for a negative size,
+ * a NULL pointer, world < 1, rank outside [0, world) or a total that
+ * overflows. */
+bwd_status bwd_zero_shard(int32_t num_tensors, const int64_t* n, int32_t world,
+                          int32_t rank, int64_t* blocks_per_rank,
+                          int32_t* num_pieces, int32_t* tensor,
+                          int64_t* offset, int64_t* count);
+
+/* ------------------------------------------------------------------------
  * Stable embedding layer (section 二 / 稳定的词嵌入层): the embedding weight
  * is initialised Xavier-uniform and a layer normalisation follows the
  * lookup, so that the layer's output has variance close to 1.
