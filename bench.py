@@ -57,6 +57,9 @@ def parse_args():
                     help="parameter storage (bf16: widened for the update, rounded back)")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--zero", action="store_true",
+                    help="ZeRO-sharded step: optimizer state split over the ranks, gradients reduce-scattered, "
+                         "parameters all-gathered (llama2_7b; strong scaling)")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the other configurations and the optimizer host-path leg (N=1 only)")
     return ap.parse_args()
@@ -726,6 +729,84 @@ def secondary_legs(dev, steps: int = 8, warmup: int = 3) -> dict:
     return legs
 
 
+def run_zero(args):
+    """The ZeRO-sharded 8-bit step on the llama2_7b set: every rank holds the
+    fp32 parameters and bf16 gradients of the whole set and the 8-bit state of
+    its own 1/N of the blocks.  One step = reduce-scatter of the gradients,
+    the fused step on the rank's pieces, all-gather of the parameters.  The
+    whole set is updated once per step whatever N is (strong scaling)."""
+    import torch
+    import torch.distributed as dist
+
+    from block_wise_dynamic_gb300 import workloads as W
+    from block_wise_dynamic_gb300.zero import ZeroAdam8bit
+
+    world, rank, local = dist_info()
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    os.environ.setdefault("MASTER_PORT", "29531")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist.init_process_group("nccl", rank=rank, world_size=world, device_id=dev)
+    wl = W.workload("llama2_7b")
+    sizes = list(wl.sizes)
+    N = sum(sizes)
+    params = [W.gen_normal(n, 0.02, seed=i, device=dev) for i, n in enumerate(sizes)]
+    opt = ZeroAdam8bit(params, lr=wl.lr, betas=(wl.beta1, wl.beta2), eps=wl.eps, grad_dtype=torch.bfloat16)
+    for i, (v, n) in enumerate(zip(opt.grad_views(), sizes)):
+        v.copy_(W.gen_normal(n, 1e-3, seed=rank * 1_000_003 + 500_000 + i, device=dev, dtype=torch.bfloat16))
+    mine = sum(c for _, _, c in opt.layout.pieces[rank])
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        opt.step()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    c0 = time.perf_counter()
+    for e in ev:
+        e[0].record(stream)
+        dist.reduce_scatter_tensor(opt.grad_shard, opt.flat_grad, op=opt.op)
+        e[1].record(stream)
+        opt.t += 1
+        opt._args.step(step=opt.t, **opt.hparams)
+        e[2].record(stream)
+        dist.all_gather_into_tensor(opt.flat_param, opt.param_shard)
+        e[3].record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    c1 = time.perf_counter()
+    clocks.stop()
+    total_ms = sum(e[0].elapsed_time(e[3]) for e in ev)
+    phase = [statistics.fmean(e[k].elapsed_time(e[k + 1]) for e in ev) for k in range(3)]
+    total_ms = max_over_ranks(total_ms, dev)
+    if rank == 0:
+        bpp = algorithmic_bytes_per_param(2, 4)
+        peak, peak_kind = measured_peak()
+        achieved = bpp * mine / (phase[1] / 1e3) / 1e9
+        line = {
+            "metric": METRIC, "value": N * args.steps / (total_ms / 1e3), "unit": "params/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "llama2_7b", "params": N, "tensors": len(sizes), "grad_dtype": "bf16",
+                       "param_dtype": "f32", "mode": "ZeRO-sharded optimizer state (reduce-scatter, step, "
+                       "all-gather)", "blocks_per_rank": opt.layout.blocks_per_rank, "params_on_rank0": mine,
+                       "parallelism": f"zero x{world}",
+                       "l2": "inputs larger than L2, no flush"},
+            "phases_ms": {"reduce_scatter": phase[0], "local_step": phase[1], "all_gather": phase[2]},
+            "roofline": {"bound": "hbm", "kernel": "adam8bit_kernel<g bf16, p f32> (rank 0's pieces)",
+                         "achieved": achieved, "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
+                         "unit": "GB/s", "frac": achieved / peak, "traffic": None, "bytes_per_param": bpp,
+                         "mean_launch_ms": phase[1]},
+            "gpu_launches": args.steps * math.ceil(len(opt.layout.pieces[rank]) / 448),
+            "clocks": clocks.summary(c0, c1),
+        }
+        print(json.dumps(line), flush=True)
+    dist.destroy_process_group()
+
+
 QUANT_BYTES_PER_ELEM = 4 + 1 + 4.0 / 2048  # fp32 in or out, one code, absmax per block
 
 
@@ -1080,6 +1161,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.zero:
+        run_zero(args)
     elif args.workload == "quant_2p28":
         run_quant(args)
     elif args.workload == "embed_7b":

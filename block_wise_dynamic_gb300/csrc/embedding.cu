@@ -21,21 +21,18 @@
 // y = (x - mean) rstd gamma + beta.  Thread 0 asks L2 for the group's next
 // row meanwhile (cp.async.bulk.prefetch.L2).
 //
-// Backward, fast path: one 768-thread CTA per SM, three groups of 256
-// threads.  Thread 0 of a group copies the weight row and the dy row of the
-// group's NEXT token into the second of two shared-memory buffers
-// (cp.async.bulk, completion counted on one mbarrier per buffer) while the
-// group works on the current token from the first: xhat from the saved mean
-// and rstd, the two sums of g = dy gamma and g xhat, then
-// dx = rstd (g - mean(g) - xhat mean(g xhat)) added into the weight row with
-// vector reductions (red.global.add.v4.f32; tokens repeat, so the adds are
-// atomic).  The rows live in shared memory, not registers, so the loads of
-// the next token overlap all of the current one's arithmetic; each thread
-// keeps dgamma and dbeta for its own columns in registers, and each CTA adds
-// the sum of its groups' partials into dgamma and dbeta once at the end
-// (0.144 ms with the rows in registers and an L2 prefetch, 0.115 ms staged,
-// on the 32,000 x 4,096 / 16,384-token case).  Other shapes take a
-// per-element path with the same arithmetic.
+// Backward, fast path: for one vocabulary row the layer's gradient is linear
+// in dL/dy, so the tokens of a row need only the sum S of their dL/dy rows
+// (one LayerNorm backward per run of equal ids instead of one per token, and
+// one atomic add of the row's dx per run).  One CTA per SM sorts a chunk of
+// consecutive tokens by id in shared memory; a producer warp streams the
+// run's dL/dy rows and then its weight row into a ring of shared-memory
+// slots (cp.async.bulk with full / empty mbarriers), sixteen consumer warps
+// sum the run in registers, reduce the two row sums once and add
+// dx = rstd (G - mean(G) - xhat mean(G xhat)), G = S gamma, into the weight
+// row's gradient with vector atomics; each consumer keeps dgamma and dbeta
+// partials for its columns and adds them once at the end.  Other shapes take
+// a per-element path with the same arithmetic, token by token.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -43,6 +40,7 @@
 #include <mutex>
 
 #include "bwd.h"
+#include "exact_div.cuh"  // packed binary32 pair arithmetic (add2, mul2, fma2)
 #include "host_util.h"
 
 namespace {
@@ -284,12 +282,10 @@ embed_bwd_slow_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const
 }
 
 // --------------------------------------------------------------------------
-// backward, fast path: rows staged in shared memory by bulk copies
-//
-// Every wait here is bounded: after about a second (or 2^24 polls) it gives
-// up, sets g_embed_fault (read and cleared by bwd_check_device), and the
-// group leaves its loop at the next group barrier after letting its copy in
-// flight land, again with a bounded wait.
+// mbarrier and bulk-copy helpers of the backward's fast path and of the
+// bounded-wait self-test.  Every wait is bounded: after about a second (or
+// 2^24 polls) it gives up and g_embed_fault is set (read and cleared by
+// bwd_check_device).
 __device__ unsigned int g_embed_fault;  // set when a bounded wait gives up
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -331,178 +327,362 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return mbar_try(a, parity) || mbar_wait_slow(a, parity);
 }
 
-constexpr int kSG = 256;                 // threads per token, staged backward
-constexpr int kSGWarps = kSG / 32;
-constexpr int kSGroups = 3;              // groups per CTA, one CTA per SM
-constexpr int kSChunks = kFastMaxDim / (4 * kSG);  // 4 float4 chunks per thread
+// Backward by runs of equal ids.  For one vocabulary row the gradient of
+// the layer is linear in dL/dy (x, mean and rstd are the row's), so the
+// tokens of that row need only the sum S of their dL/dy rows: one LayerNorm
+// backward on S gives the row's summed dx, and S xhat and S are its shares of
+// dgamma and dbeta.  Each CTA (one per SM) takes a chunk of consecutive
+// tokens, sorts its (id, position) pairs in shared memory, and walks the
+// runs of equal ids in ascending id order.  Two consumer groups of seven
+// warps take alternate runs, so one group's row reduction overlaps the other
+// group's streaming; each group has its own ring of shared-memory slots and
+// its own producer warp, which copies the group's runs, each run's dL/dy rows
+// and then its weight row, into the ring (cp.async.bulk; a "full" mbarrier
+// per slot counts the bytes, an "empty" one the consumer warps that released
+// it; one consumer per ring, so every wait is on the slot's next phase).  A
+// group adds the run's dL/dy rows into S in registers,
+// and at the weight row reduces the two row sums once and adds dx into the
+// row's gradient with vector atomics (other chunks may hold the same id).
+// Every CTA visits ids in ascending order, so a row that several SMs touch
+// is touched at about the same time and stays in L2; the streamed dL/dy rows
+// are copied with an L2 evict-first policy.
+//
+// Every wait is bounded (about a second, or 2^24 polls).  A wait that gives
+// up sets the device fault word and the CTA's fail flag; from then on every
+// wait of the CTA returns at once and the producer issues no more copies, so
+// all threads run the same barriers to the end; before the CTA exits, the
+// producers wait (bounded) for the last copy they issued into each slot.
+constexpr int kRGroups = 2;                          // consumer groups, alternate runs
+constexpr int kRGT = 224;                            // threads per consumer group (7 warps)
+constexpr int kRGWarps = kRGT / 32;
+constexpr int kRCons = kRGroups * kRGT;
+constexpr int kRThreads = kRCons + 32 * kRGroups;    // + a producer warp per group: 16 warps, 128 registers
+constexpr int kRChunks = (kFastMaxDim / 4 + kRGT - 1) / kRGT;  // float4 chunks per consumer thread (5)
+constexpr int kRChunkMax = 1024;                     // tokens sorted per chunk
+constexpr int kRRingBytes = 160 * 1024;
+constexpr int kRSlotsMax = 16;                       // per group
+constexpr long long kRNoId = 0x7fffffffffffffffLL;   // sort key of an id outside [0, V)
 
-__host__ __device__ constexpr int staged_smem_bytes(int dim) { return kSGroups * 2 * 2 * dim * 4; }
-
-__device__ __forceinline__ void group_sync256(int group) {
-  asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "n"(kSG) : "memory");
+// slots per group ring
+__host__ __device__ constexpr int runs_slots(int dim) {
+  return kRRingBytes / (kRGroups * dim * 4) < kRSlotsMax ? kRRingBytes / (kRGroups * dim * 4) : kRSlotsMax;
+}
+// the two rings, gamma, then the sort keys, positions and per-position statistics
+__host__ __device__ constexpr int runs_smem_bytes(int dim) {
+  return kRGroups * runs_slots(dim) * dim * 4 + dim * 4 + kRChunkMax * (8 + 4 + 4 + 4);
 }
 
-template <int kVals>
-__device__ __forceinline__ void group_sum256(float (&v)[kVals], float* red, int slot, int group, int t) {
-  const int lane = t & 31, warp = t >> 5;
-#pragma unroll
-  for (int i = 0; i < kVals; ++i) v[i] = warp_sum(v[i]);
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < kVals; ++i) red[(slot * kVals + i) * kSGWarps + warp] = v[i];
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Bounded wait that also gives up at once when the CTA's fail flag is set;
+// a wait that runs out sets the flag and the device fault word.
+__device__ __forceinline__ bool mbar_wait_or_fail(uint64_t* bar, uint32_t parity, volatile int* fail) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try(a, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < (1u << 24); ++i) {
+    if (mbar_try(a, parity)) return true;
+    if (*fail) return false;
+    if (global_ns() - t0 > 1000000000ull) break;
   }
-  group_sync256(group);
-#pragma unroll
-  for (int i = 0; i < kVals; ++i) {
-    const float4 a = *reinterpret_cast<const float4*>(&red[(slot * kVals + i) * kSGWarps]);
-    const float4 b = *reinterpret_cast<const float4*>(&red[(slot * kVals + i) * kSGWarps + 4]);
-    v[i] = __fadd_rn(__fadd_rn(__fadd_rn(a.x, a.y), __fadd_rn(a.z, a.w)), __fadd_rn(__fadd_rn(b.x, b.y), __fadd_rn(b.z, b.w)));
+  *fail = 1;
+  atomicOr(&g_embed_fault, 1u);
+  return false;
+}
+
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy) : "memory");
+}
+
+// Named barrier of consumer group g (barrier 0 is __syncthreads).
+__device__ __forceinline__ void rgroup_sync(int g) {
+  asm volatile("bar.sync %0, %1;" ::"r"(g + 1), "n"(kRGT) : "memory");
+}
+
+// Next ring position: slot index and the parity of its current round.
+__device__ __forceinline__ void ring_next(int& slot, uint32_t& phase, int nslots) {
+  if (++slot == nslots) {
+    slot = 0;
+    phase ^= 1u;
   }
 }
 
-// Backward with the rows staged in shared memory: thread 0 of each group
-// copies the next token's weight and dy rows (cp.async.bulk, one mbarrier
-// per buffer) while the group works on the current token from the other
-// buffer; dgamma / dbeta partials stay in registers.
-__global__ void __launch_bounds__(kSG * kSGroups, 1)
-embed_bwd_staged_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const float* __restrict__ w, int64_t vocab,
-                        int dim, const float* __restrict__ gamma, const float* __restrict__ mean,
-                        const float* __restrict__ rstd, const float* __restrict__ dy, float* __restrict__ dw,
-                        float* __restrict__ dgamma, float* __restrict__ dbeta) {
-  extern __shared__ __align__(128) float s_buf[];  // [group][buffer][x | dy][dim]
-  __shared__ __align__(16) float s_red[kSGroups][2 * 2 * kSGWarps];
-  __shared__ __align__(8) uint64_t s_full[kSGroups][2];
-  // s_abort[group][c]: a wait gave up in an iteration of parity 1 - c.  All
-  // threads read cell (it & 1) right after the loop-top barrier of
-  // iteration it.  Writes to that cell come from iteration it - 1, finished
-  // before that barrier, or from iteration it + 1, which no thread enters
-  // before every thread has reached the next loop-top barrier, after its
-  // read: so all threads of the group decide alike.
-  __shared__ int s_abort[kSGroups][2];
-  const int group = threadIdx.x / kSG, t = threadIdx.x % kSG;
+__global__ void __launch_bounds__(kRThreads, 1)
+embed_bwd_runs_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const float* __restrict__ w,
+                      int64_t vocab, int dim, const float* __restrict__ gamma, const float* __restrict__ mean,
+                      const float* __restrict__ rstd, const float* __restrict__ dy, float* __restrict__ dw,
+                      float* __restrict__ dgamma, float* __restrict__ dbeta, int chunk, int vec_gb) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  const int nslots = runs_slots(dim);
+  float* const s_gamma = reinterpret_cast<float*>(smem_raw) + static_cast<size_t>(kRGroups) * nslots * dim;
+  long long* const s_key = reinterpret_cast<long long*>(s_gamma + dim);
+  int* const s_pos = reinterpret_cast<int*>(s_key + kRChunkMax);
+  float* const s_mu = reinterpret_cast<float*>(s_pos + kRChunkMax);
+  float* const s_rs = s_mu + kRChunkMax;
+  __shared__ __align__(8) uint64_t s_full_all[kRGroups][kRSlotsMax];
+  __shared__ __align__(8) uint64_t s_empty_all[kRGroups][kRSlotsMax];
+  __shared__ __align__(16) float s_red[kRGroups][2][2][8];  // warp partials, entry 7 stays 0
+  __shared__ int s_nvalid;
+  __shared__ int s_fail_flag;
+  volatile int* const s_fail = &s_fail_flag;
+
+  const int tid = threadIdx.x, lane = tid & 31;
+  const bool producer = tid >= kRCons;
+  // group served (consumers: their group; producers: warp kRCons/32 + g feeds group g),
+  // and a consumer's thread and warp within its group
+  const int grp = producer ? (tid - kRCons) / 32 : tid / kRGT;
+  const int gt = tid % kRGT, gw = gt >> 5;
+  float* const ring = reinterpret_cast<float*>(smem_raw) + static_cast<size_t>(grp) * nslots * dim;
+  uint64_t* const s_full = s_full_all[grp];
+  uint64_t* const s_empty = s_empty_all[grp];
   const int nch = dim >> 2;
   const float fdim = static_cast<float>(dim);
   const uint32_t row_bytes = static_cast<uint32_t>(dim) * 4u;
-  float* const gbuf = s_buf + static_cast<int64_t>(group) * 4 * dim;
-  if (t == 0) {
-    mbar_init(&s_full[group][0], 1);
-    mbar_init(&s_full[group][1], 1);
-    s_abort[group][0] = s_abort[group][1] = 0;
-  }
-  __syncthreads();
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kSGroups;
-  const int64_t tok0 = static_cast<int64_t>(blockIdx.x) * kSGroups + group;
-  // copies of token `tok` into buffer `b` (nothing for an id outside [0, V));
-  // thread 0 counts the phases it started per buffer (for the drain below)
-  uint32_t issued[2] = {0u, 0u};
-  auto issue = [&](int64_t tok, int b) {
-    const int64_t id = ids[tok];
-    if (id < 0 || id >= vocab) return;
-    ++issued[b];
-    uint64_t* bar = &s_full[group][b];
-    mbar_expect_tx(bar, 2u * row_bytes);
-    bulk_g2s(gbuf + b * 2 * dim, w + id * static_cast<int64_t>(dim), row_bytes, bar);
-    bulk_g2s(gbuf + b * 2 * dim + dim, dy + tok * static_cast<int64_t>(dim), row_bytes, bar);
-  };
-  if (t == 0 && tok0 < num_tokens) issue(tok0, 0);
-  float4 pg[kSChunks], pb[kSChunks];
-#pragma unroll
-  for (int k = 0; k < kSChunks; ++k) pg[k] = pb[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  uint32_t phase = 0;  // bit b: parity of buffer b's next phase
-  int slot = 0;
-  int it = 0;
-  for (int64_t tok = tok0; tok < num_tokens; tok += stride, ++it) {
-    const int b = it & 1;
-    group_sync256(group);  // every thread is done with the other buffer
-    if (s_abort[group][it & 1]) break;
-    if (t == 0 && tok + stride < num_tokens) issue(tok + stride, b ^ 1);
-    const int64_t id = ids[tok];
-    if (id < 0 || id >= vocab) continue;  // the whole group skips together
-    const bool ok = mbar_wait(&s_full[group][b], (phase >> b) & 1u);
-    phase ^= 1u << b;
-    if (!ok) {
-      atomicOr(&g_embed_fault, 1u);
-      s_abort[group][(it + 1) & 1] = 1;
+  if (tid == 0) {
+    for (int g = 0; g < kRGroups; ++g) {
+      for (int i = 0; i < nslots; ++i) {
+        mbar_init(&s_full_all[g][i], 1);
+        mbar_init(&s_empty_all[g][i], kRGWarps);  // released by the group's warps
+      }
     }
-    const float mu = mean[tok], r = rstd[tok];
-    const float* xs = gbuf + b * 2 * dim;
-    const float* ds = xs + dim;
-    float s[2] = {0.0f, 0.0f};
+    s_fail_flag = 0;
+    for (int i = 0; i < kRGroups * 2 * 2 * 8; ++i) (&s_red[0][0][0][0])[i] = 0.0f;
+  }
+  for (int c = tid; c < nch; c += kRThreads)
+    reinterpret_cast<float4*>(s_gamma)[c] = ldg4(gamma + 4 * c);
+  __syncthreads();
+
+  // producer state (lane 0 of each producer warp)
+  uint64_t evict_first = 0;
+  if (producer && lane == 0) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
+  uint32_t walked = 0;      // ring items walked (a failure stops the copies, not the walk)
+  uint32_t used = 0, last_par = 0;  // per slot: ever filled, parity of its last fill
+  // position in the group's ring, walked alike by its producer and consumers
+  int slot = 0;
+  uint32_t phase = 0;
+  uint32_t run = 0;         // runs seen so far; run r belongs to group r & 1
+  float4 S[kRChunks], pg[kRChunks], pb[kRChunks];
 #pragma unroll
-    for (int k = 0; k < kSChunks; ++k) {
-      const int c = t + kSG * k;
-      if (c < nch) {
-        const float4 x = *reinterpret_cast<const float4*>(xs + 4 * c);
-        const float4 d = *reinterpret_cast<const float4*>(ds + 4 * c);
-        const float4 g = ldg4(gamma + 4 * c);
-        const float4 xh = make_float4(__fmul_rn(__fsub_rn(x.x, mu), r), __fmul_rn(__fsub_rn(x.y, mu), r),
-                                      __fmul_rn(__fsub_rn(x.z, mu), r), __fmul_rn(__fsub_rn(x.w, mu), r));
-        const float4 gg = make_float4(__fmul_rn(d.x, g.x), __fmul_rn(d.y, g.y), __fmul_rn(d.z, g.z), __fmul_rn(d.w, g.w));
-        s[0] = __fadd_rn(s[0], __fadd_rn(__fadd_rn(gg.x, gg.y), __fadd_rn(gg.z, gg.w)));
-        s[1] = __fadd_rn(s[1], __fadd_rn(__fadd_rn(__fmul_rn(gg.x, xh.x), __fmul_rn(gg.y, xh.y)),
-                                         __fadd_rn(__fmul_rn(gg.z, xh.z), __fmul_rn(gg.w, xh.w))));
-        if (ok) {
-          pg[k].x = __fadd_rn(pg[k].x, __fmul_rn(d.x, xh.x));
-          pg[k].y = __fadd_rn(pg[k].y, __fmul_rn(d.y, xh.y));
-          pg[k].z = __fadd_rn(pg[k].z, __fmul_rn(d.z, xh.z));
-          pg[k].w = __fadd_rn(pg[k].w, __fmul_rn(d.w, xh.w));
-          pb[k].x = __fadd_rn(pb[k].x, d.x);
-          pb[k].y = __fadd_rn(pb[k].y, d.y);
-          pb[k].z = __fadd_rn(pb[k].z, d.z);
-          pb[k].w = __fadd_rn(pb[k].w, d.w);
+  for (int k = 0; k < kRChunks; ++k) S[k] = pg[k] = pb[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  int red_par = 0;
+
+  const int64_t nchunks = (num_tokens + chunk - 1) / chunk;
+  for (int64_t ch = blockIdx.x; ch < nchunks; ch += gridDim.x) {
+    const int64_t c0 = ch * chunk;
+    const int cnt = static_cast<int>(num_tokens - c0 < chunk ? num_tokens - c0 : chunk);
+    int p2 = 1;
+    while (p2 < cnt) p2 <<= 1;
+    // (id, position) keys; ids outside [0, V) sort last and are left out
+    for (int i = tid; i < p2; i += kRThreads) {
+      long long key = kRNoId;
+      if (i < cnt) {
+        const int64_t id = ids[c0 + i];
+        if (id >= 0 && id < vocab) key = id;
+        s_mu[i] = mean[c0 + i];  // by position in the chunk, read with the ids
+        s_rs[i] = rstd[c0 + i];
+      }
+      s_key[i] = key;
+      s_pos[i] = i;
+    }
+    if (tid == 0) s_nvalid = 0;
+    __syncthreads();
+    // bitonic sort of the pairs, ascending by id, then position
+    for (int k = 2; k <= p2; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < p2; i += kRThreads) {
+          const int l = i ^ j;
+          if (l > i) {
+            const long long ki = s_key[i], kl = s_key[l];
+            const int pi = s_pos[i], pl = s_pos[l];
+            const bool gt2 = ki > kl || (ki == kl && pi > pl);
+            if (gt2 == ((i & k) == 0)) {
+              s_key[i] = kl; s_key[l] = ki;
+              s_pos[i] = pl; s_pos[l] = pi;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = tid; i < p2; i += kRThreads)
+      if (s_key[i] != kRNoId && (i + 1 == p2 || s_key[i + 1] == kRNoId)) s_nvalid = i + 1;
+    __syncthreads();
+    const int nv = s_nvalid;
+
+    if (producer) {
+      if (lane == 0) {
+        auto issue = [&](const float* src, bool stream) {
+          if (walked >= static_cast<uint32_t>(nslots)) mbar_wait_or_fail(&s_empty[slot], phase ^ 1u, s_fail);
+          if (!*s_fail) {  // the flag never clears: after a failure no copy starts
+            mbar_expect_tx(&s_full[slot], row_bytes);
+            if (stream) bulk_g2s_hint(ring + static_cast<size_t>(slot) * dim, src, row_bytes, &s_full[slot], evict_first);
+            else bulk_g2s(ring + static_cast<size_t>(slot) * dim, src, row_bytes, &s_full[slot]);
+            used |= 1u << slot;
+            last_par = (last_par & ~(1u << slot)) | (phase << slot);
+          }
+          ++walked;
+          ring_next(slot, phase, nslots);
+        };
+        for (int j = 0; j < nv; ++j) {
+          const bool mine = static_cast<int>(run & 1u) == grp;
+          if (mine) issue(dy + (c0 + s_pos[j]) * static_cast<int64_t>(dim), true);
+          if (j + 1 == nv || s_key[j + 1] != s_key[j]) {
+            if (mine) issue(w + s_key[j] * static_cast<int64_t>(dim), false);
+            ++run;
+          }
+        }
+      }
+    } else {
+      for (int j = 0; j < nv; ++j) {
+        const bool mine = static_cast<int>(run & 1u) == grp;
+        if (mine) {  // a dL/dy row of this group's run: S += row
+          mbar_wait_or_fail(&s_full[slot], phase, s_fail);
+          const float* row = ring + static_cast<size_t>(slot) * dim;
+#pragma unroll
+          for (int k = 0; k < kRChunks; ++k) {
+            const int c = gt + kRGT * k;
+            if (c < nch) {
+              const float4 d = ld4(row + 4 * c);
+              const float2 lo = bwd::add2(make_float2(S[k].x, S[k].y), make_float2(d.x, d.y));
+              const float2 hi = bwd::add2(make_float2(S[k].z, S[k].w), make_float2(d.z, d.w));
+              S[k] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[slot]);
+          ring_next(slot, phase, nslots);
+        }
+        if (j + 1 < nv && s_key[j + 1] == s_key[j]) continue;
+        ++run;
+        if (!mine) continue;  // the other group's run
+        // the run's weight row: one LayerNorm backward on S
+        mbar_wait_or_fail(&s_full[slot], phase, s_fail);
+        const float* xs = ring + static_cast<size_t>(slot) * dim;
+        const int pj = s_pos[j];
+        const float r = s_rs[pj];
+        const float2 r2 = bwd::dup2(r), nmu2 = bwd::dup2(-s_mu[pj]);
+        // per element pair: xhat = (x - mean) r, G = S gamma, sums of G and G xhat
+        float2 xh[2 * kRChunks], G[2 * kRChunks];
+        float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < kRChunks; ++k) {
+          const int c = gt + kRGT * k;
+          if (c < nch) {
+            const float4 x = ld4(xs + 4 * c);
+            const float4 g4 = ld4(s_gamma + 4 * c);
+            xh[2 * k] = bwd::mul2(bwd::add2(make_float2(x.x, x.y), nmu2), r2);
+            xh[2 * k + 1] = bwd::mul2(bwd::add2(make_float2(x.z, x.w), nmu2), r2);
+            G[2 * k] = bwd::mul2(make_float2(S[k].x, S[k].y), make_float2(g4.x, g4.y));
+            G[2 * k + 1] = bwd::mul2(make_float2(S[k].z, S[k].w), make_float2(g4.z, g4.w));
+            a0 = bwd::add2(a0, bwd::add2(G[2 * k], G[2 * k + 1]));
+            a1 = bwd::fma2(G[2 * k], xh[2 * k], bwd::fma2(G[2 * k + 1], xh[2 * k + 1], a1));
+          } else {
+            xh[2 * k] = xh[2 * k + 1] = G[2 * k] = G[2 * k + 1] = make_float2(0.0f, 0.0f);
+          }
+        }
+        float s2[2] = {__fadd_rn(a0.x, a0.y), __fadd_rn(a1.x, a1.y)};
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[slot]);
+        ring_next(slot, phase, nslots);
+        s2[0] = warp_sum(s2[0]);
+        s2[1] = warp_sum(s2[1]);
+        if (lane == 0) {
+          s_red[grp][red_par][0][gw] = s2[0];
+          s_red[grp][red_par][1][gw] = s2[1];
+        }
+        rgroup_sync(grp);
+        float tot[2];
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          const float4 a = *reinterpret_cast<const float4*>(&s_red[grp][red_par][v][0]);
+          const float4 b = *reinterpret_cast<const float4*>(&s_red[grp][red_par][v][4]);
+          tot[v] = __fadd_rn(__fadd_rn(__fadd_rn(a.x, a.y), __fadd_rn(a.z, a.w)),
+                             __fadd_rn(__fadd_rn(b.x, b.y), __fadd_rn(b.z, b.w)));
+        }
+        red_par ^= 1;
+        // dx = r (G - m1 - xhat m2) = G r + (xhat (-m2 r) - m1 r), m the row means of G and G xhat
+        const float m1 = __fdiv_rn(tot[0], fdim), m2 = __fdiv_rn(tot[1], fdim);
+        const float2 nm2r = bwd::dup2(-__fmul_rn(m2, r)), nm1r = bwd::dup2(-__fmul_rn(m1, r));
+        float* dwrow = dw + s_key[j] * static_cast<int64_t>(dim);
+#pragma unroll
+        for (int k = 0; k < kRChunks; ++k) {
+          const int c = gt + kRGT * k;
+          if (c < nch) {
+            const float2 d0 = bwd::fma2(G[2 * k], r2, bwd::fma2(xh[2 * k], nm2r, nm1r));
+            const float2 d1 = bwd::fma2(G[2 * k + 1], r2, bwd::fma2(xh[2 * k + 1], nm2r, nm1r));
+            red_add4(dwrow + 4 * c, make_float4(d0.x, d0.y, d1.x, d1.y));
+            const float2 g0 = bwd::fma2(make_float2(S[k].x, S[k].y), xh[2 * k], make_float2(pg[k].x, pg[k].y));
+            const float2 g1 = bwd::fma2(make_float2(S[k].z, S[k].w), xh[2 * k + 1], make_float2(pg[k].z, pg[k].w));
+            pg[k] = make_float4(g0.x, g0.y, g1.x, g1.y);
+            const float2 b0 = bwd::add2(make_float2(S[k].x, S[k].y), make_float2(pb[k].x, pb[k].y));
+            const float2 b1 = bwd::add2(make_float2(S[k].z, S[k].w), make_float2(pb[k].z, pb[k].w));
+            pb[k] = make_float4(b0.x, b0.y, b1.x, b1.y);
+          }
+          S[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
       }
     }
-    group_sum256<2>(s, s_red[group], slot, group, t);
-    slot ^= 1;
-    const float m1 = __fdiv_rn(s[0], fdim), m2 = __fdiv_rn(s[1], fdim);
-    float* dwrow = dw + id * static_cast<int64_t>(dim);
+    __syncthreads();  // the next chunk's keys overwrite this one's
+  }
+  // After a failure, let the last copy issued into each slot land (bounded)
+  // before the rings' shared memory is reused below.
+  if (producer && lane == 0 && *s_fail) {
+    for (int i = 0; i < nslots; ++i)
+      if ((used >> i) & 1u) mbar_wait(&s_full[i], (last_par >> i) & 1u);
+  }
+  // dgamma / dbeta: group 1's partials join group 0's through shared memory
+  // (the rings are idle now), then one add per column per CTA.  Every CTA
+  // adds into the same 2 x D floats at about the same time, so the adds are
+  // vector reductions where dgamma and dbeta are 16-byte aligned, and each
+  // CTA starts at its own column so concurrent adds fall on different L2
+  // lines.
+  __syncthreads();
+  float4* const xpg = reinterpret_cast<float4*>(smem_raw);
+  float4* const xpb = xpg + nch;
+  if (!producer && grp == 1) {
 #pragma unroll
-    for (int k = 0; k < kSChunks; ++k) {
-      const int c = t + kSG * k;
-      if (c < nch && ok) {
-        const float4 x = *reinterpret_cast<const float4*>(xs + 4 * c);
-        const float4 d = *reinterpret_cast<const float4*>(ds + 4 * c);
-        const float4 g = ldg4(gamma + 4 * c);
-        float4 dx;
-        dx.x = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d.x, g.x), m1), __fmul_rn(__fmul_rn(__fsub_rn(x.x, mu), r), m2)));
-        dx.y = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d.y, g.y), m1), __fmul_rn(__fmul_rn(__fsub_rn(x.y, mu), r), m2)));
-        dx.z = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d.z, g.z), m1), __fmul_rn(__fmul_rn(__fsub_rn(x.z, mu), r), m2)));
-        dx.w = __fmul_rn(r, __fsub_rn(__fsub_rn(__fmul_rn(d.w, g.w), m1), __fmul_rn(__fmul_rn(__fsub_rn(x.w, mu), r), m2)));
-        red_add4(dwrow + 4 * c, dx);
+    for (int k = 0; k < kRChunks; ++k) {
+      const int c = gt + kRGT * k;
+      if (c < nch) {
+        xpg[c] = pg[k];
+        xpb[c] = pb[k];
       }
     }
   }
-  // A group that gave up lets every copy it started land (bounded) before
-  // the buffers are reused below: the one whose wait timed out and the one
-  // issued ahead.  The k-th copy into a buffer completes its phase k - 1;
-  // waiting on the parity of a phase that already completed returns at once.
-  if (t == 0 && (s_abort[group][0] || s_abort[group][1])) {
-#pragma unroll
-    for (int b = 0; b < 2; ++b)
-      if (issued[b] > 0) mbar_wait(&s_full[group][b], (issued[b] - 1u) & 1u);
-  }
   __syncthreads();
-  // partials: each group's into its first buffer, then summed over the groups in order
-  float* const part = s_buf + static_cast<int64_t>(group) * 4 * dim;
+  if (!producer && grp == 0) {
+    const int rot = static_cast<int>((static_cast<int64_t>(blockIdx.x) * nch) / gridDim.x);
 #pragma unroll
-  for (int k = 0; k < kSChunks; ++k) {
-    const int c = t + kSG * k;
-    if (c < nch) {
-      *reinterpret_cast<float4*>(part + 4 * c) = pg[k];
-      *reinterpret_cast<float4*>(part + dim + 4 * c) = pb[k];
+    for (int k = 0; k < kRChunks; ++k) {
+      const int c0 = gt + kRGT * k;
+      if (c0 < nch) {
+        const float4 og = xpg[c0], ob = xpb[c0];
+        const float4 tg = make_float4(__fadd_rn(pg[k].x, og.x), __fadd_rn(pg[k].y, og.y), __fadd_rn(pg[k].z, og.z),
+                                      __fadd_rn(pg[k].w, og.w));
+        const float4 tb = make_float4(__fadd_rn(pb[k].x, ob.x), __fadd_rn(pb[k].y, ob.y), __fadd_rn(pb[k].z, ob.z),
+                                      __fadd_rn(pb[k].w, ob.w));
+        xpg[c0] = tg;
+        xpb[c0] = tb;
+      }
     }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < dim; i += blockDim.x) {
-    float a = 0.0f, bsum = 0.0f;
-#pragma unroll
-    for (int gi = 0; gi < kSGroups; ++gi) {
-      a = __fadd_rn(a, s_buf[static_cast<int64_t>(gi) * 4 * dim + i]);
-      bsum = __fadd_rn(bsum, s_buf[static_cast<int64_t>(gi) * 4 * dim + dim + i]);
+    rgroup_sync(0);
+    for (int i = gt; i < nch; i += kRGT) {
+      const int c = i + rot < nch ? i + rot : i + rot - nch;
+      const float4 tg = xpg[c], tb = xpb[c];
+      if (vec_gb) {
+        red_add4(dgamma + 4 * c, tg);
+        red_add4(dbeta + 4 * c, tb);
+      } else {  // dgamma and dbeta need only 4-byte alignment
+        atomicAdd(dgamma + 4 * c, tg.x); atomicAdd(dgamma + 4 * c + 1, tg.y);
+        atomicAdd(dgamma + 4 * c + 2, tg.z); atomicAdd(dgamma + 4 * c + 3, tg.w);
+        atomicAdd(dbeta + 4 * c, tb.x); atomicAdd(dbeta + 4 * c + 1, tb.y);
+        atomicAdd(dbeta + 4 * c + 2, tb.z); atomicAdd(dbeta + 4 * c + 3, tb.w);
+      }
     }
-    atomicAdd(dgamma + i, a);
-    atomicAdd(dbeta + i, bsum);
   }
 }
 
@@ -545,8 +725,8 @@ bwd_status ensure_device(EmbedDevice** out) {
     d.ready = false;
     if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute");
-    if ((e = cudaFuncSetAttribute(reinterpret_cast<const void*>(embed_bwd_staged_kernel),
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, staged_smem_bytes(kFastMaxDim))) !=
+    if ((e = cudaFuncSetAttribute(reinterpret_cast<const void*>(embed_bwd_runs_kernel),
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, runs_smem_bytes(kFastMaxDim))) !=
         cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
     struct { const void* fn; int threads; int* out; } occ[] = {
@@ -682,10 +862,15 @@ bwd_status bwd_embedding_backward(const int64_t* ids, int64_t num_tokens, const 
   const bool fast = dim % 4 == 0 && dim <= kFastMaxDim && aligned16(weight) && aligned16(gamma) &&
                     aligned16(dy) && aligned16(dweight);
   if (fast) {
-    embed_bwd_staged_kernel<<<grid_for(num_tokens, kSGroups, d->num_sms, 1), kSG * kSGroups,
-                              staged_smem_bytes(static_cast<int>(dim)), st>>>(
-        ids, num_tokens, weight, num_embeddings, static_cast<int>(dim), gamma, mean, rstd, dy, dweight, dgamma, dbeta);
-    return check_launch("embed_bwd_staged_kernel launch");
+    // one CTA per SM, each on chunks of consecutive tokens (at most 1,024)
+    int64_t chunk = (num_tokens + d->num_sms - 1) / d->num_sms;
+    if (chunk > kRChunkMax) chunk = kRChunkMax;
+    const int64_t nchunks = (num_tokens + chunk - 1) / chunk;
+    const int grid = static_cast<int>(nchunks < d->num_sms ? nchunks : d->num_sms);
+    embed_bwd_runs_kernel<<<grid, kRThreads, runs_smem_bytes(static_cast<int>(dim)), st>>>(
+        ids, num_tokens, weight, num_embeddings, static_cast<int>(dim), gamma, mean, rstd, dy, dweight, dgamma, dbeta,
+        static_cast<int>(chunk), aligned16(dgamma) && aligned16(dbeta) ? 1 : 0);
+    return check_launch("embed_bwd_runs_kernel launch");
   }
   embed_bwd_slow_kernel<<<grid_for(num_tokens, kSlowGroups, d->num_sms, d->occ_slow_bwd), kGroup * kSlowGroups, 0,
                           st>>>(ids, num_tokens, weight, num_embeddings, dim, gamma, mean, rstd, dy, dweight, dgamma,

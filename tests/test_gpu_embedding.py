@@ -311,9 +311,9 @@ def test_full_size_embed_7b_sampled(E):
         assert np.all(np.abs(got.cpu().numpy() - ref) <= tol)
 
 
-def test_device_check_after_staged_backward(E):
-    """The staged backward's bounded waits complete in normal operation: the
-    device fault flag stays clear."""
+def test_device_check_after_backward(E):
+    """The backward's bounded waits complete in normal operation: the device
+    fault flag stays clear."""
     import block_wise_dynamic_gb300 as bwd
 
     d, v = 4096, 500
@@ -325,6 +325,55 @@ def test_device_check_after_staged_backward(E):
     for _ in range(3):
         E.backward(ids, w, g, mean, rstd, dy, torch.zeros_like(w), torch.zeros_like(g), torch.zeros_like(g))
     bwd.check_device(0)
+
+
+@pytest.mark.parametrize("case", ["many_chunks", "one_id", "all_distinct", "one_token", "two_tokens"])
+def test_backward_runs_of_equal_ids(E, case):
+    """The fast path sums the dL/dy rows of each run of equal ids within a
+    chunk of tokens (at most 1,024 per chunk, chunks spread over the SMs):
+    more tokens than one pass of chunks holds, every token on one id (one
+    long run per chunk), every id distinct (runs of one), and one or two
+    tokens."""
+    rng = np.random.default_rng(80)
+    if case == "many_chunks":
+        v, d, ids = 3000, 64, ids_for(200_000, 3000, 81)
+    elif case == "one_id":
+        v, d, ids = 50, 512, np.full(20_000, 17, dtype=np.int64)
+    elif case == "all_distinct":
+        v, d = 6000, 1024
+        ids = rng.permutation(v)[:5000].astype(np.int64)
+    elif case == "one_token":
+        v, d, ids = 10, 4096, np.array([7], dtype=np.int64)
+    else:
+        v, d, ids = 10, 4096, np.array([7, 7], dtype=np.int64)
+    w = rand_weight(v, d, 82)
+    gamma, _ = affine(d, 83)
+    dy = rng.standard_normal((ids.size, d))
+    check_backward(E, w, gamma, ids, dy)
+
+
+def test_backward_with_unaligned_dgamma_dbeta(E):
+    """The fast path with dgamma and dbeta placed one float into larger
+    buffers (4-byte but not 16-byte aligned): the end-of-kernel adds take the
+    scalar form."""
+    d, v, t = 4096, 300, 2000
+    w = rand_weight(v, d, 90)
+    gamma, _ = affine(d, 91)
+    ids = ids_for(t, v, 92)
+    dy = np.random.default_rng(93).standard_normal((t, d)).astype(np.float32)
+    wd, gd = torch.from_numpy(w).to(dev()), torch.from_numpy(gamma).to(dev())
+    ids_d = torch.from_numpy(ids).to(dev())
+    _, mean, rstd = E.forward(ids_d, wd, gd, torch.zeros_like(gd))
+    gb = torch.zeros(2 * d + 2, device=dev())
+    dg, db = gb[1:1 + d], gb[d + 2:]
+    assert dg.data_ptr() % 16 == 4
+    E.backward(ids_d, wd, gd, mean, rstd, torch.from_numpy(dy).to(dev()), torch.zeros_like(wd), dg, db)
+    torch.cuda.synchronize()
+    dy64 = dy.astype(np.float64)
+    _, rg, rb = se.backward(ids, w, gamma, dy64)
+    _, sg, sb = se.backward_abs_sums(ids, w, gamma, dy64)
+    for got, ref, s_ in ((dg, rg, sg), (db, rb, sb)):
+        assert np.all(np.abs(got.cpu().numpy() - ref) <= 2 * (128 + t) * U * s_ + 1e-30)
 
 
 def test_backward_with_many_interleaved_invalid_ids(E):

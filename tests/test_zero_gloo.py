@@ -1,0 +1,111 @@
+"""The ZeRO-sharded step's collective plumbing on CPU ranks (gloo, world
+sizes 2 and 3): reduce-scatter of the flat gradient buffer, the rank's local
+step on its pieces, all-gather of the parameters.  The local step here is the
+oracle's 8-bit step (test only); after several steps every rank's parameters,
+and the rank-owned states, equal the unsharded oracle run on the summed
+gradients bit for bit.  Gradients are multiples of 2^-20 below 2^-8, so their
+sums are exact in any order and every rank agrees on them."""
+
+import os
+import socket
+import sys
+
+import numpy as np
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SIZES = [5000, 2048 * 3, 17, 0, 9000, 2048]
+STEPS = 3
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _grad(i, n, rank, step):
+    rng = np.random.default_rng(1000 * step + 37 * rank + i)
+    return (rng.integers(-2 ** 12, 2 ** 12, n) * 2.0 ** -20).astype(np.float32)
+
+
+def _param(i, n):
+    return (np.random.default_rng(i).standard_normal(n) * 0.02).astype(np.float32)
+
+
+def _rank(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import oracle
+    from block_wise_dynamic_gb300.zero import ZeroAdam8bit
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    params = [torch.from_numpy(_param(i, n)) for i, n in enumerate(SIZES)]
+    states = {}
+
+    def oracle_local(pv, gv, t, hp):
+        for j, (p, g) in enumerate(zip(pv, gv)):
+            st = states.setdefault(j, oracle.state_init(p.numel()))
+            res = oracle.adam8bit_step(p.numpy().copy(), g.numpy().copy(), *st,
+                                       oracle.AdamHParams(lr=hp["lr"], step=t))
+            p.copy_(torch.from_numpy(res[0]))
+            states[j] = res[1:]
+
+    opt = ZeroAdam8bit(params, lr=1e-3, reduce_op="sum", local_step=oracle_local)
+    for step in range(1, STEPS + 1):
+        opt.zero_grad()
+        for i, (g, n) in enumerate(zip(opt.grad_views(), SIZES)):
+            g.copy_(torch.from_numpy(_grad(i, n, rank, step)))
+        opt.step()
+    out[rank] = ([p.numpy().copy() for p in params], opt.layout.pieces[rank],
+                 {j: tuple(np.asarray(x).copy() for x in s) for j, s in states.items()})
+    dist.destroy_process_group()
+
+
+def _unsharded(world):
+    sys.path.insert(0, ROOT)
+    import oracle
+
+    ps = [_param(i, n) for i, n in enumerate(SIZES)]
+    sts = [oracle.state_init(n) for n in SIZES]
+    for step in range(1, STEPS + 1):
+        for i, n in enumerate(SIZES):
+            g = np.zeros(n, np.float32)
+            for r in range(world):
+                g = g + _grad(i, n, r, step)
+            res = oracle.adam8bit_step(ps[i], g, *sts[i], oracle.AdamHParams(lr=1e-3, step=step))
+            ps[i], sts[i] = res[0], res[1:]
+    return ps, sts
+
+
+def _check(world):
+    port = _free_port()
+    with mp.get_context("spawn").Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_rank, args=(world, port, out), nprocs=world, join=True)
+        got = dict(out)
+    ref_p, ref_st = _unsharded(world)
+    for r in range(world):
+        params, pieces, states = got[r]
+        for a, b in zip(params, ref_p):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+        for j, (ti, off, cnt) in enumerate(pieces):
+            mc, ma, vc, va = states[j]
+            rmc, rma, rvc, rva = ref_st[ti]
+            b0, b1 = off // 2048, -(-(off + cnt) // 2048)
+            assert np.array_equal(mc, rmc[off:off + cnt]) and np.array_equal(vc, rvc[off:off + cnt])
+            assert np.array_equal(ma.view(np.uint32), rma[b0:b1].view(np.uint32))
+            assert np.array_equal(va.view(np.uint32), rva[b0:b1].view(np.uint32))
+    assert sum(len(got[r][1]) for r in range(world)) >= len([n for n in SIZES if n])
+
+
+def test_zero_step_gloo_world2_matches_unsharded_oracle():
+    _check(2)
+
+
+def test_zero_step_gloo_world3_matches_unsharded_oracle():
+    _check(3)
