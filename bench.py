@@ -1135,7 +1135,7 @@ def run_embed(args):
         },
         "passes": per,
         "hbm_gbs": (nbytes["forward"] + nbytes["backward"]) / (elapsed_ms / args.steps / 1e3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "embed_bwd_kernel" if dom == "backward" else "embed_fwd_kernel",
+        "roofline": {"bound": "hbm", "kernel": "embed_bwd_runs_kernel" if dom == "backward" else "embed_fwd_kernel",
                      "achieved": achieved, "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
                      "unit": "GB/s", "frac": achieved / peak, "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
                      "traffic": None if tr is None or dom not in tr else tr[dom],
