@@ -646,8 +646,23 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
     const float ma_old = T.ma[lb];
     const float va_old = T.va[lb];
     // four threads ask L2 for the group's next block, one array each, so
-    // that block's loads find it there instead of in DRAM
-    if (t < 4) {
+    // that block's loads find it there instead of in DRAM.  With 16-bit
+    // parameters (a step bound by instruction issue) only a next block in
+    // the same tensor is prefetched, which needs no tensor search (13.05
+    // against 13.20 ms per 7B step); with fp32 parameters (bound by DRAM)
+    // the first block of the next tensor is prefetched too (14.24 against
+    // 14.31 ms).
+    if (kP != kF32) {
+      if (t < 4) {
+        const int64_t bn = base + stride * BWD_BLOCK;
+        if (T.vec && T.n - bn >= BWD_BLOCK) {
+          if (t == 0) prefetch_l2(static_cast<const char*>(T.p) + bn * elem_bytes<kP>(), BWD_BLOCK * elem_bytes<kP>());
+          else if (t == 1) prefetch_l2(static_cast<const char*>(T.g) + bn * elem_bytes<kG>(), BWD_BLOCK * elem_bytes<kG>());
+          else if (t == 2) prefetch_l2(T.mc + bn, 2048u);
+          else prefetch_l2(T.vc + bn, 2048u);
+        }
+      }
+    } else if (t < 4) {
       const int64_t gn = gb + stride;
       if (gn < total) {
         while (args.block_start[tn + 1] <= gn) ++tn;
