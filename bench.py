@@ -460,20 +460,26 @@ def run_ours(args):
         pipe.step(step=t, **hp)  # one untimed step: first use of the streams and host pages
         torch.cuda.synchronize(dev)
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fe = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
         barrier()
         torch.cuda.synchronize(dev)
         f0.record(stream)
-        for _ in range(args.e2e_steps):
+        fe[0].record(stream)
+        for k in range(args.e2e_steps):
             t += 1
             pipe.step(step=t, **hp)
+            fe[k + 1].record(stream)
         f1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
         e2e_ms = f0.elapsed_time(f1)
+        e2e_step_ms = [fe[k].elapsed_time(fe[k + 1]) for k in range(args.e2e_steps)]
         e2e_ms = max_over_ranks(e2e_ms, dev)
         e2e = {"value": world * N * args.e2e_steps / (e2e_ms / 1e3), "unit": "params/s",
                "h2d_bytes_per_step": N * gbytes, "d2h_bytes_per_step": N * pbytes,
                "steps": args.e2e_steps,
+               "step_ms": {"min": min(e2e_step_ms), "median": statistics.median(e2e_step_ms),
+                           "max": max(e2e_step_ms)},
                "what": "per step through block_wise_dynamic_gb300.offload.PipelinedHostStep: gradients "
                        "H2D from pinned host memory, the 8-bit step, updated fp32 parameters D2H into "
                        "pinned host memory, pipelined over 256 MiB chunks on three streams, after one "
@@ -767,12 +773,11 @@ def run_zero(args):
     c0 = time.perf_counter()
     for e in ev:
         e[0].record(stream)
-        dist.reduce_scatter_tensor(opt.grad_shard, opt.flat_grad, op=opt.op)
+        opt.reduce_gradients()
         e[1].record(stream)
-        opt.t += 1
-        opt._args.step(step=opt.t, **opt.hparams)
+        opt.local_update()
         e[2].record(stream)
-        dist.all_gather_into_tensor(opt.flat_param, opt.param_shard)
+        opt.gather_parameters()
         e[3].record(stream)
     torch.cuda.synchronize(dev)
     dist.barrier()

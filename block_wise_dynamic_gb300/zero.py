@@ -146,20 +146,35 @@ class ZeroAdam8bit:
     def zero_grad(self) -> None:
         self.flat_grad.zero_()
 
-    @torch.no_grad()
-    def step(self, async_gather: bool = False):
-        """Reduce-scatter, local 8-bit step, all-gather.  With
-        ``async_gather`` the gather is left in flight and its work handle
-        returned (wait on it before the parameters are read)."""
+    def reduce_gradients(self) -> None:
+        """Phase 1: reduce-scatter the flat gradients; this rank's shard of
+        the reduced gradients lands in ``grad_shard``."""
         dist.reduce_scatter_tensor(self.grad_shard, self.flat_grad, op=self.op, group=self.group)
+
+    @torch.no_grad()
+    def local_update(self) -> None:
+        """Phase 2: the 8-bit Adam step on this rank's pieces (one
+        multi-tensor launch of the library's fused kernel)."""
         t = self.t + 1
         if self.local_step is not None:
             self.local_step(self.piece_params, self.piece_grads, t, dict(self.hparams))
         elif self._args is not None:
             self._args.step(step=t, **self.hparams)
         self.t = t
-        work = dist.all_gather_into_tensor(self.flat_param, self.param_shard, group=self.group,
-                                           async_op=async_gather)
+
+    def gather_parameters(self, async_op: bool = False):
+        """Phase 3: all-gather the updated parameter shards in place; with
+        ``async_op`` the work handle of the gather in flight is returned."""
+        return dist.all_gather_into_tensor(self.flat_param, self.param_shard, group=self.group, async_op=async_op)
+
+    @torch.no_grad()
+    def step(self, async_gather: bool = False):
+        """Reduce-scatter, local 8-bit step, all-gather.  With
+        ``async_gather`` the gather is left in flight and its work handle
+        returned (wait on it before the parameters are read)."""
+        self.reduce_gradients()
+        self.local_update()
+        work = self.gather_parameters(async_op=async_gather)
         return work if async_gather else None
 
     def state_dict(self) -> dict:
