@@ -46,15 +46,21 @@ def _tensors(seed, gdt):
 
 
 def _bits(t):
-    return t.cpu().view(torch.int32).numpy() if t.dtype == torch.float32 else t.cpu().numpy()
+    if t.dtype == torch.float32:
+        return t.cpu().view(torch.int32).numpy()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.cpu().view(torch.int16).numpy()
+    return t.cpu().numpy()
 
 
 @pytest.mark.parametrize("world", [2, 3, 8])
-@pytest.mark.parametrize("gdt", [torch.bfloat16, torch.float32])
-def test_sharded_steps_equal_the_unsharded_step(bwd, world, gdt):
+@pytest.mark.parametrize("gdt,pdt", [(torch.bfloat16, torch.float32), (torch.float32, torch.float32),
+                                     (torch.bfloat16, torch.bfloat16)])
+def test_sharded_steps_equal_the_unsharded_step(bwd, world, gdt, pdt):
     from block_wise_dynamic_gb300.zero import ShardLayout
 
     ps, gsteps = _tensors(11, gdt)
+    ps = [p.to(pdt) for p in ps]
     ref = [p.clone() for p in ps]
     ref_st = [bwd.state_init(n, DEV) for n in SIZES]
     L = ShardLayout(SIZES, world)
