@@ -347,6 +347,43 @@ def test_optimizer_skipped_gradients_and_failed_step(bwd):
         compare_step(got, tuple(r))
 
 
+def test_optimizer_parameter_groups_with_their_own_hyperparameters(bwd):
+    """AdamW8bit over two parameter groups with different lr and weight
+    decay (the second one bf16): each group's launches use its own
+    hyperparameters, checked against the oracle per tensor."""
+    torch.manual_seed(4)
+    g1 = [torch.nn.Parameter(torch.randn(n, device=DEV) * 0.02) for n in (3000, 2048)]
+    g2 = [torch.nn.Parameter((torch.randn(n, device=DEV) * 0.02).to(torch.bfloat16)) for n in (5000,)]
+    opt = bwd.AdamW8bit([{"params": g1, "lr": 2e-3, "weight_decay": 0.1},
+                         {"params": g2, "lr": 5e-4, "weight_decay": 0.0}])
+
+    def bits16(t):
+        return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    ref = {id(p): ((p.detach().cpu().numpy().copy() if p.dtype == torch.float32 else bits16(p)),
+                   *oracle.state_init(p.numel())) for p in g1 + g2}
+    for t in range(1, 4):
+        for p in g1 + g2:
+            p.grad = (torch.randn(p.numel(), device=DEV) * 1e-2).to(p.dtype)
+        opt.step()
+        for p, lr, wd in [(q, 2e-3, 0.1) for q in g1] + [(q, 5e-4, 0.0) for q in g2]:
+            hp = oracle.AdamHParams(lr=lr, weight_decay=wd, step=t)
+            ref[id(p)] = oracle.adam8bit_step(*ref[id(p)][:1], g_to_np(p.grad), *ref[id(p)][1:], hp,
+                                              p_bf16=p.dtype == torch.bfloat16)
+    for p in g1 + g2:
+        st = opt.state[p]
+        r = ref[id(p)]
+        codes = (st["m_codes"].cpu().numpy(), st["m_absmax"].cpu().numpy(), st["v_codes"].cpu().numpy(),
+                 st["v_absmax"].cpu().numpy())
+        if p.dtype == torch.float32:
+            compare_step((p.detach().cpu().numpy(), *codes), r)
+        else:  # bf16 parameters: rounded fp32 updates; the states are exact
+            compare_bf16_params(bits16(p), r[0])
+            for c, rc in zip(codes, r[1:]):
+                assert np.array_equal(c.view(np.uint8), rc.view(np.uint8))
+        assert st["step"] == 3
+
+
 def test_step_on_tensor_larger_than_2p31_elements(bwd):
     """64-bit indexing in the fused step: one tensor of 2^31 + 5 parameters;
     blocks at the 2^31 boundary and the ragged tail against the oracle."""

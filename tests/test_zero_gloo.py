@@ -109,3 +109,67 @@ def test_zero_step_gloo_world2_matches_unsharded_oracle():
 
 def test_zero_step_gloo_world3_matches_unsharded_oracle():
     _check(3)
+
+
+def _rank_autograd(rank, world, port, out):
+    """A small model on each rank: autograd writes the gradients straight
+    into the optimizer's flat buffer (p.grad are views of it)."""
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import oracle
+    from block_wise_dynamic_gb300.zero import ZeroAdam8bit
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    torch.manual_seed(0)
+    model = torch.nn.Sequential(torch.nn.Linear(48, 70), torch.nn.Tanh(), torch.nn.Linear(70, 5))
+    params = list(model.parameters())
+    states = {}
+
+    def oracle_local(pv, gv, t, hp):
+        for j, (p, g) in enumerate(zip(pv, gv)):
+            st = states.setdefault(j, oracle.state_init(p.numel()))
+            res = oracle.adam8bit_step(p.numpy().copy(), g.numpy().copy(), *st, oracle.AdamHParams(lr=hp["lr"], step=t))
+            p.copy_(torch.from_numpy(res[0]))
+            states[j] = res[1:]
+
+    opt = ZeroAdam8bit(params, lr=1e-2, reduce_op="sum", local_step=oracle_local)
+    flat = opt.flat_grad
+    grads_seen = []
+    for step in range(2):
+        opt.zero_grad()
+        x = torch.from_numpy(np.random.default_rng(10 * step + rank).standard_normal((16, 48)).astype(np.float32))
+        model(x).square().mean().backward()
+        assert all(p.grad.data_ptr() >= flat.data_ptr() for p in params)  # still views of the flat buffer
+        grads_seen.append([p.grad.detach().clone().numpy() for p in params])
+        opt.step()
+    out[rank] = ([p.detach().numpy().copy() for p in params], grads_seen)
+    dist.destroy_process_group()
+
+
+def test_zero_step_takes_autograd_gradients_from_its_flat_buffer():
+    """Two gloo ranks, a real backward pass each: every rank ends with the
+    parameters of the unsharded oracle run on the sum of both ranks'
+    gradients (the model and seeds are the same on both ranks)."""
+    sys.path.insert(0, ROOT)
+    import oracle
+
+    port = _free_port()
+    with mp.get_context("spawn").Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_rank_autograd, args=(2, port, out), nprocs=2, join=True)
+        got = dict(out)
+    torch.manual_seed(0)
+    model = torch.nn.Sequential(torch.nn.Linear(48, 70), torch.nn.Tanh(), torch.nn.Linear(70, 5))
+    ps = [p.detach().numpy().reshape(-1).copy() for p in model.parameters()]
+    sts = [oracle.state_init(p.size) for p in ps]
+    for step in range(2):
+        for i in range(len(ps)):
+            g = (got[0][1][step][i].reshape(-1) + got[1][1][step][i].reshape(-1)).astype(np.float32)
+            res = oracle.adam8bit_step(ps[i], g, *sts[i], oracle.AdamHParams(lr=1e-2, step=step + 1))
+            ps[i], sts[i] = res[0], res[1:]
+    for r in (0, 1):
+        for a, b in zip(got[r][0], ps):
+            assert np.array_equal(a.reshape(-1).view(np.uint32), b.view(np.uint32))
