@@ -104,6 +104,8 @@ class ZeroAdam8bit:
         devices = {p.device for p in params}
         if len(dtypes) != 1 or len(devices) != 1:
             raise TypeError("all parameters must share one dtype and one device")
+        if len({id(p) for p in params}) != len(params):
+            raise ValueError("a parameter appears more than once")
         if reduce_op not in ("avg", "sum"):
             raise ValueError("reduce_op must be 'avg' or 'sum'")
         self.group = group
@@ -125,8 +127,9 @@ class ZeroAdam8bit:
                 n = p.numel()
                 self.flat_param[off:off + n].copy_(p.detach().reshape(-1))
                 p.data = self.flat_param[off:off + n].view_as(p)
-                if gdt == pdt:
-                    p.grad = self.flat_grad[off:off + n].view_as(p)
+                # a gradient left elsewhere would be ignored by the step: either a
+                # view of the flat buffer or nothing (then use grad_views())
+                p.grad = self.flat_grad[off:off + n].view_as(p) if gdt == pdt else None
         s0 = self.rank * L.shard_numel
         self.param_shard = self.flat_param[s0:s0 + L.shard_numel]
         mine = L.pieces[self.rank]

@@ -173,3 +173,40 @@ def test_zero_step_takes_autograd_gradients_from_its_flat_buffer():
     for r in (0, 1):
         for a, b in zip(got[r][0], ps):
             assert np.array_equal(a.reshape(-1).view(np.uint32), b.view(np.uint32))
+
+
+def _rank_checks(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    from block_wise_dynamic_gb300.zero import ZeroAdam8bit
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    a = torch.nn.Parameter(torch.zeros(10))
+    b = torch.nn.Parameter(torch.zeros(3000))
+    a.grad = torch.ones(10)
+    res = []
+    try:
+        ZeroAdam8bit([a, b, a], reduce_op="sum", local_step=lambda *x: None)
+        res.append("duplicate accepted")
+    except ValueError:
+        res.append("duplicate rejected")
+    opt = ZeroAdam8bit([a, b], reduce_op="sum", grad_dtype=torch.float64, local_step=lambda *x: None)
+    res.append(a.grad is None and b.grad is None)
+    res.append(opt.grad_views()[1].dtype == torch.float64 and opt.grad_views()[1].shape == b.shape)
+    out[rank] = res
+    dist.destroy_process_group()
+
+
+def test_zero_driver_argument_checks():
+    """A parameter listed twice is refused; with a gradient dtype other than
+    the parameters', stale gradients are cleared (the step reads only the
+    flat buffer, through grad_views())."""
+    port = _free_port()
+    with mp.get_context("spawn").Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_rank_checks, args=(2, port, out), nprocs=2, join=True)
+        got = dict(out)
+    assert got[0] == got[1] == ["duplicate rejected", True, True]
