@@ -10,12 +10,12 @@
 //
 // Work decomposition.  A group of 128 threads owns one 2048-element block at a
 // time and the groups walk the blocks with a grid stride (grid = SMs x
-// resident CTAs).  The fused step runs one 768-thread CTA of six groups per
-// SM (80 registers x 768 threads fill the register file), so the code tables
-// sit in shared memory once per SM and leave the rest of the unified array
-// to L1 for the loads in flight (three 256-thread CTAs per SM, each with its
-// own copy, ran 4% slower); the standalone quantizer runs two CTAs of four
-// groups.  Thread t of a group owns the 16 elements 4 t + 512 k + j (k, j < 4)
+// resident CTAs).  The fused step runs one CTA per SM, of seven groups with
+// fp32 parameters and six with 16-bit ones (the register file divided among
+// them: 72 and 80 registers a thread), so the code tables sit in shared
+// memory once per SM and leave the rest of the unified array to L1 for the
+// loads in flight (three 256-thread CTAs per SM, each with its own copy, ran
+// 4% slower); the standalone quantizer runs two CTAs of four groups.  Thread t of a group owns the 16 elements 4 t + 512 k + j (k, j < 4)
 // of its block ("quads" of 4 elements, 4 x 128 = 512 elements apart), so
 // every warp-wide load or store touches one contiguous span (512 B of fp32,
 // 256 B of bf16, 128 B of codes) and is fully coalesced.  The block absmax is
@@ -60,8 +60,9 @@ constexpr int kPer = BWD_BLOCK / kGroup;      // 16 elements per thread
 constexpr int kQuads = kPer / 4;              // 4-element quads per thread
 constexpr int kSpan = 4 * kGroup;             // elements between a thread's quads
 constexpr int kGroupWarps = kGroup / 32;      // 4
-constexpr int kGroups = 6;                    // blocks in flight per CTA (Adam), one CTA per SM
-constexpr int kCta = kGroup * kGroups;        // 768 threads
+// Adam: blocks in flight per CTA, one CTA per SM (adam_groups below): seven
+// 128-thread groups (896 threads, 72 registers) with fp32 parameters, six
+// (768 threads, 80 registers) with 16-bit ones.
 constexpr int kQGroups = 4;                   // blocks in flight per CTA (quantize)
 constexpr int kQCta = kGroup * kQGroups;      // 512 threads
 constexpr int kDeqThreads = 256;              // dequantize: 8 elements per thread
@@ -612,11 +613,20 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
   return r;
 }
 
+// Groups per CTA of the fused step.  The DRAM-bound fp32-parameter step runs
+// seven (14.13 against 14.24 ms per 7B step with six; eight spill more and
+// run 14.49); the issue-bound 16-bit-parameter step keeps six, whose 80
+// registers hold its lookups without spills (seven: 12.97, eight: 13.13,
+// against 12.94 ms).
+template <int kP>
+__host__ __device__ constexpr int adam_groups() { return kP == kF32 ? 7 : 6; }
+
 // kG: gradient type; kP: parameter type (kF32, kBF16 or kF16; 16-bit
 // parameters are widened for the update and rounded back on store).
 template <int kG, int kP>
-__global__ void __launch_bounds__(kCta, 1)
+__global__ void __launch_bounds__(kGroup * adam_groups<kP>(), 1)
 adam8bit_kernel(const __grid_constant__ AdamArgs args) {
+  constexpr int kGroups = adam_groups<kP>();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   bwd::Tables& tab = *reinterpret_cast<bwd::Tables*>(smem_raw);
   __shared__ __align__(16) float s_red[kGroups][2 * 2 * kGroupWarps];
@@ -937,7 +947,9 @@ bwd_status ensure_device(DeviceState** out) {
     if ((s = occupancy(kd[k], kDeqThreads, 0, &d.occ_dequant[k])) != BWD_OK) return s;
   }
   for (int k = 0; k < 9; ++k)
-    if ((s = occupancy(ka[k], kCta, kTablesBytes, &d.occ_adam[k])) != BWD_OK) return s;
+    if ((s = occupancy(ka[k], kGroup * (k < 3 ? adam_groups<kF32>() : adam_groups<kBF16>()), kTablesBytes,
+                       &d.occ_adam[k])) != BWD_OK)
+      return s;
   d.ctx = ctx;
   d.ready = true;
   *out = &d;
@@ -985,13 +997,14 @@ void fill_scalars(const bwd_adam_hparams* hp, AdamArgs* a) {
 
 template <int kG, int kP>
 void launch_typed(const AdamArgs& a, int grid, cudaStream_t st) {
-  adam8bit_kernel<kG, kP><<<grid, kCta, kTablesBytes, st>>>(a);
+  adam8bit_kernel<kG, kP><<<grid, kGroup * adam_groups<kP>(), kTablesBytes, st>>>(a);
 }
 
 bwd_status launch_adam_chunk(const AdamArgs& a, int g_type, int p_type, const DeviceState& d, cudaStream_t st) {
   const int64_t total = a.block_start[a.num_tensors];
   if (total == 0) return BWD_OK;
-  const int grid = grid_for(total, kGroups, d, d.occ_adam[3 * p_type + g_type]);
+  const int grid = grid_for(total, p_type == BWD_F32 ? adam_groups<kF32>() : adam_groups<kBF16>(), d,
+                            d.occ_adam[3 * p_type + g_type]);
   switch (3 * p_type + g_type) {
     case 0: launch_typed<kF32, kF32>(a, grid, st); break;
     case 1: launch_typed<kBF16, kF32>(a, grid, st); break;
