@@ -118,11 +118,12 @@ __device__ __forceinline__ int64_t rem_in_block(int64_t n, int64_t base) {
 
 __device__ __forceinline__ uint32_t byte_of(uint32_t w, int k) { return (w >> (8 * k)) & 0xffu; }
 
-// The same byte by one byte permute (PRMT); the 16-bit-parameter step, bound
-// by instruction issue, uses it for its dequantizing lookups (12.82 against
-// 13.07 ms per 7B step with bf16 gradients; with fp16 gradients it would
-// spill), the DRAM-bound fp32 one keeps the shift-and-mask form (14.24
-// against 14.30 ms with the permute).
+// The same byte by one byte permute (PRMT), which the fused step uses for its
+// dequantizing lookups: 16-bit parameters 12.82 against 13.07 ms per 7B step,
+// fp32 parameters with bf16 gradients (seven groups per SM) 13.98 against
+// 14.13 ms.  Two instantiations keep the shift-and-mask form: fp16 gradients
+// (the permutes spill) and fp32 parameters with fp32 gradients (17.13 against
+// 16.98 ms).
 __device__ __forceinline__ uint32_t byte_prmt(uint32_t w, int k) {
   return __byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(k));
 }
@@ -739,7 +740,7 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
     const float2 eps2 = bwd::dup2(eps), nstep2 = bwd::dup2(-step_size), decay2 = bwd::dup2(decay);
 #pragma unroll
     for (int j = 0; j < kPer; j += 2) {
-      constexpr bool kPerm = kP != kF32 && kG != kF16;  // fp16 gradients: the permutes spill
+      constexpr bool kPerm = kG != kF16 && !(kG == kF32 && kP == kF32);
       const uint32_t im0 = kPerm ? byte_prmt(mw[j >> 2], j & 3) : byte_of(mw[j >> 2], j & 3);
       const uint32_t im1 = kPerm ? byte_prmt(mw[j >> 2], (j & 3) + 1) : byte_of(mw[j >> 2], (j & 3) + 1);
       const uint32_t iv0 = kPerm ? byte_prmt(vw[j >> 2], j & 3) : byte_of(vw[j >> 2], j & 3);
