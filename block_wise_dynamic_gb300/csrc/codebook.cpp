@@ -116,6 +116,8 @@ int make_entry(const float* t, float v_lo, float v_hi, uint32_t shift, uint32_t 
 
 int build_entries(const float* ts, const float* tu, uint32_t* ent, char* err, size_t errlen) {
   for (int i = 0; i < kEntries; ++i) ent[i] = 255u << kEntShift;  // padding, never read
+  // each stored word is the bucket's E less its lookup word's top bits
+  // (tables.h), so that entry + lookup word = E + low bits
   for (uint32_t h = kSgnLo; h <= kSgnHi; ++h) {
     // the first bucket of each sign also takes every smaller magnitude
     // (down to +0.0, and down to the smallest negative subnormal: -0.0 is
@@ -123,23 +125,28 @@ int build_entries(const float* ts, const float* tu, uint32_t* ent, char* err, si
     const float top = from_bits((h << kSgnShift) | kSgnLowMask);
     const float pos_lo = h == kSgnLo ? 0.0f : from_bits(h << kSgnShift);
     const float neg_hi = h == kSgnLo ? -from_bits(1u) : -from_bits(h << kSgnShift);
-    if (make_entry(ts, pos_lo, top, kSgnShift, kSgnLowMask, false, &ent[h - kSgnLo], err, errlen) != 0 ||
-        make_entry(ts, -top, neg_hi, kSgnShift, kSgnLowMask, true, &ent[kSgnN + h - kSgnLo], err, errlen) != 0)
+    const uint32_t jn = h ^ kSgnIdxFlip;  // index of the negative bucket
+    uint32_t ep, en;
+    if (make_entry(ts, pos_lo, top, kSgnShift, kSgnLowMask, false, &ep, err, errlen) != 0 ||
+        make_entry(ts, -top, neg_hi, kSgnShift, kSgnLowMask, true, &en, err, errlen) != 0)
       return -1;
+    ent[h - kSgnBase] = ep - (h << kSgnShift);
+    ent[jn - kSgnBase] = en - (jn << kSgnShift);
   }
   for (uint32_t h = kUnsLo; h <= kUnsHi; ++h) {
     const float lo = h == kUnsLo ? 0.0f : from_bits(h << kUnsShift);
-    if (make_entry(tu, lo, from_bits((h << kUnsShift) | kUnsLowMask), kUnsShift, kUnsLowMask, false,
-                   &ent[kUnsOff + h - kUnsLo], err, errlen) != 0)
+    uint32_t e;
+    if (make_entry(tu, lo, from_bits((h << kUnsShift) | kUnsLowMask), kUnsShift, kUnsLowMask, false, &e, err,
+                   errlen) != 0)
       return -1;
+    ent[kUnsOff + h - kUnsLo] = e - (h << kUnsShift);
   }
   // Unsigned quantization divides by the block absmax without a
   // tiny-quotient check (exact_div.cuh, unscaled form), so a quotient below
-  // 2^-63 may come out with either sign; the non-negative lookup then reads
-  // the first bucket's entry with arbitrary low bits.  That gives code 0, the
-  // code of every such quotient, only while the first bucket holds no
-  // threshold.
-  if (ent[kUnsOff] != (1u << kEntShift) - (1u << kSgnShift)) {
+  // 2^-63 may come out with either sign; the lookup clamps it into the first
+  // bucket.  That gives code 0, the code of every such quotient, only while
+  // the first bucket holds no threshold.
+  if (ent[kUnsOff] + (kUnsLo << kUnsShift) != (1u << kEntShift) - (1u << kSgnShift)) {
     std::snprintf(err, errlen, "the first unsigned bucket holds a threshold");
     return -1;
   }

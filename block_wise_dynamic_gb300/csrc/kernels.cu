@@ -179,21 +179,20 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 // beside an infinite absmax.  So |q| <= 1 or q is a quiet NaN, and the only
 // clamp needed is the lower one, which also sends NaN (fmaxf returns the
 // other operand) to the first bucket: every lookup stays in the table.
+// The lookup word x carries the table index in its top bits and the low
+// bits below them; one logic operation folds the sign into both.
 __device__ __forceinline__ uint32_t code_word_signed(float q, const bwd::Tables& tab) {
-  const uint32_t b = __float_as_uint(q);
-  const uint32_t h = __float_as_uint(fmaxf(fabsf(q), __uint_as_float(bwd::kSgnLo << bwd::kSgnShift))) >>
-                     bwd::kSgnShift;
-  const uint32_t i = h - bwd::kSgnLo + ((b >> 31) ? bwd::kSgnN : 0u);
-  const uint32_t low = (b ^ static_cast<uint32_t>(static_cast<int32_t>(b) >> 31)) & bwd::kSgnLowMask;
-  return tab.ent[i] + low;
+  const uint32_t m = __float_as_uint(fmaxf(fabsf(q), __uint_as_float(bwd::kSgnLo << bwd::kSgnShift)));
+  const uint32_t s = static_cast<uint32_t>(static_cast<int32_t>(__float_as_uint(q)) >> 31);
+  const uint32_t x = m ^ (s & bwd::kSgnFlip);
+  return tab.ent[(x >> bwd::kSgnShift) - bwd::kSgnBase] + x;
 }
 
 // Unsigned map, q in [+0, 1] or NaN (the second moment is never negative;
 // same range argument as above).
 __device__ __forceinline__ uint32_t code_word_unsigned_nonneg(float q, const bwd::Tables& tab) {
-  const uint32_t b = __float_as_uint(q);
-  const uint32_t h = __float_as_uint(fmaxf(q, __uint_as_float(bwd::kUnsLo << bwd::kUnsShift))) >> bwd::kUnsShift;
-  return tab.ent[bwd::kUnsOff - bwd::kUnsLo + h] + (b & bwd::kUnsLowMask);
+  const uint32_t x = __float_as_uint(fmaxf(q, __uint_as_float(bwd::kUnsLo << bwd::kUnsShift)));
+  return tab.ent[bwd::kUnsOff - bwd::kUnsLo + (x >> bwd::kUnsShift)] + x;
 }
 
 // Unsigned map, any sign: every threshold is positive, so a negative input
@@ -616,11 +615,35 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
 
 // Groups per CTA of the fused step.  The DRAM-bound fp32-parameter step runs
 // seven (14.13 against 14.24 ms per 7B step with six; eight spill more and
-// run 14.49); the issue-bound 16-bit-parameter step keeps six, whose 80
-// registers hold its lookups without spills (seven: 12.97, eight: 13.13,
-// against 12.94 ms).
+// run 14.49).  The issue-bound 16-bit-parameter step: six with bf16
+// parameters, whose 80 registers hold the lookups without spills (seven:
+// 12.43, five: 12.85, against 12.26 ms), seven with fp16 ones (12.20
+// against 12.28 ms with six).
 template <int kP>
-__host__ __device__ constexpr int adam_groups() { return kP == kF32 ? 7 : 6; }
+__host__ __device__ constexpr int adam_groups() { return kP == kBF16 ? 6 : 7; }
+
+// With 16-bit parameters (a step bound by instruction issue) the
+// dequantizing lookups read lane-private copies of both maps: entry c of
+// lane l's copy is word 32 c + l, in bank l, so the 32 lookups of a warp
+// never share a bank (random codes in one 256-word map take about three
+// shared-memory wavefronts per warp lookup): 12.25 against 12.67 ms per 7B
+// step.  The DRAM-bound fp32-parameter step reads the maps themselves (with
+// the copies 14.1 against 13.98 ms).  64 KB beside the 28 KB of tables; one
+// CTA per SM either way.
+constexpr int kLanes = 32;
+constexpr int kRepBytes = 2 * bwd::kCodes * kLanes * 4;
+template <int kP>
+__host__ __device__ constexpr bool adam_rep() { return kP != kF32; }
+template <int kP>
+__host__ __device__ constexpr int adam_smem() { return kTablesBytes + (adam_rep<kP>() ? kRepBytes : 0); }
+
+// The same two numbers for a runtime parameter type (bwd_dtype).
+int adam_groups_of(int p_type) {
+  return p_type == BWD_F32 ? adam_groups<kF32>() : p_type == BWD_BF16 ? adam_groups<kBF16>() : adam_groups<kF16>();
+}
+int adam_smem_of(int p_type) {
+  return p_type == BWD_F32 ? adam_smem<kF32>() : p_type == BWD_BF16 ? adam_smem<kBF16>() : adam_smem<kF16>();
+}
 
 // kG: gradient type; kP: parameter type (kF32, kBF16 or kF16; 16-bit
 // parameters are widened for the update and rounded back on store).
@@ -630,9 +653,19 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
   constexpr int kGroups = adam_groups<kP>();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   bwd::Tables& tab = *reinterpret_cast<bwd::Tables*>(smem_raw);
+  float4* rep4 = reinterpret_cast<float4*>(smem_raw + kTablesBytes);
   __shared__ __align__(16) float s_red[kGroups][2 * 2 * kGroupWarps];
+  constexpr bool kRep = adam_rep<kP>();
   copy_to_smem(&tab, &g_tables, kTablesBytes);
   __syncthreads();
+  if (kRep) {
+    const float* maps = &tab.map[0][0];  // both maps, 2 x 256 contiguous floats
+    for (int i = threadIdx.x; i < kRepBytes / 16; i += blockDim.x) {
+      const float v = maps[i >> 3];  // 8 float4 = 32 lanes per entry
+      rep4[i] = make_float4(v, v, v, v);
+    }
+    __syncthreads();
+  }
 
   const int group = threadIdx.x / kGroup, t = threadIdx.x % kGroup;
   const int nt = args.num_tensors;
@@ -652,8 +685,9 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
 
   const float b1 = args.b1, omb1 = args.omb1, b2 = args.b2, omb2 = args.omb2;
   const float eps = args.eps, step_size = args.step_size, inv_bc2s = args.inv_bc2s, decay = args.decay;
-  const float* map_s = tab.map[0];
-  const float* map_u = tab.map[1];
+  constexpr int kStride = kRep ? kLanes : 1;  // words between a map's entries
+  const float* map_s = kRep ? reinterpret_cast<const float*>(rep4) + (threadIdx.x & (kLanes - 1)) : tab.map[0];
+  const float* map_u = kRep ? map_s + bwd::kCodes * kLanes : tab.map[1];
 
   int it = 0;
   for (; gb < total; gb += stride, ++it) {
@@ -745,8 +779,8 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
       const uint32_t im1 = kPerm ? byte_prmt(mw[j >> 2], (j & 3) + 1) : byte_of(mw[j >> 2], (j & 3) + 1);
       const uint32_t iv0 = kPerm ? byte_prmt(vw[j >> 2], j & 3) : byte_of(vw[j >> 2], j & 3);
       const uint32_t iv1 = kPerm ? byte_prmt(vw[j >> 2], (j & 3) + 1) : byte_of(vw[j >> 2], (j & 3) + 1);
-      const float2 mo = bwd::mul2(make_float2(map_s[im0], map_s[im1]), ma2);
-      const float2 vo = bwd::mul2(make_float2(map_u[iv0], map_u[iv1]), va2);
+      const float2 mo = bwd::mul2(make_float2(map_s[im0 * kStride], map_s[im1 * kStride]), ma2);
+      const float2 vo = bwd::mul2(make_float2(map_u[iv0 * kStride], map_u[iv1 * kStride]), va2);
       const float2 g2 = make_float2(g[j], g[j + 1]);
       // products packed, sums scalar: a packed multiply feeding a packed add
       // may be contracted into one fused operation, which would change the
@@ -948,8 +982,7 @@ bwd_status ensure_device(DeviceState** out) {
     if ((s = occupancy(kd[k], kDeqThreads, 0, &d.occ_dequant[k])) != BWD_OK) return s;
   }
   for (int k = 0; k < 9; ++k)
-    if ((s = occupancy(ka[k], kGroup * (k < 3 ? adam_groups<kF32>() : adam_groups<kBF16>()), kTablesBytes,
-                       &d.occ_adam[k])) != BWD_OK)
+    if ((s = occupancy(ka[k], kGroup * adam_groups_of(k / 3), adam_smem_of(k / 3), &d.occ_adam[k])) != BWD_OK)
       return s;
   d.ctx = ctx;
   d.ready = true;
@@ -998,14 +1031,13 @@ void fill_scalars(const bwd_adam_hparams* hp, AdamArgs* a) {
 
 template <int kG, int kP>
 void launch_typed(const AdamArgs& a, int grid, cudaStream_t st) {
-  adam8bit_kernel<kG, kP><<<grid, kGroup * adam_groups<kP>(), kTablesBytes, st>>>(a);
+  adam8bit_kernel<kG, kP><<<grid, kGroup * adam_groups<kP>(), adam_smem<kP>(), st>>>(a);
 }
 
 bwd_status launch_adam_chunk(const AdamArgs& a, int g_type, int p_type, const DeviceState& d, cudaStream_t st) {
   const int64_t total = a.block_start[a.num_tensors];
   if (total == 0) return BWD_OK;
-  const int grid = grid_for(total, p_type == BWD_F32 ? adam_groups<kF32>() : adam_groups<kBF16>(), d,
-                            d.occ_adam[3 * p_type + g_type]);
+  const int grid = grid_for(total, adam_groups_of(p_type), d, d.occ_adam[3 * p_type + g_type]);
   switch (3 * p_type + g_type) {
     case 0: launch_typed<kF32, kF32>(a, grid, st); break;
     case 1: launch_typed<kBF16, kF32>(a, grid, st); break;

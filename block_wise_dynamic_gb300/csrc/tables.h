@@ -14,30 +14,50 @@
 //   bits of q are >= those of t; for negative values the order of the low
 //   bits is reversed, so they are complemented first ("low" below).
 //
-//   entries.  One 32-bit word per bucket, E = c * 2^24 + (2^24 - tl), with tl
-//   the (complemented, for negative buckets) low bits of the bucket's
-//   threshold, or 2^17 when the bucket has none.  For any low < 2^17,
+//   entries.  Per bucket E = c * 2^24 + (2^24 - tl), with tl the
+//   (complemented, for negative buckets) low bits of the bucket's threshold,
+//   or 2^17 when the bucket has none.  For any low < 2^17,
 //       code(q) = (E + low(q)) >> 24,  the top byte of the sum,
 //   because 2^24 - tl + low lies in [2^24 - 2^17, 2^24 + 2^17) and reaches
 //   2^24 exactly when low >= tl.  The sum stays below 2^32: a bucket with
 //   c = 255 has no threshold left (E = 2^32 - 2^17), and for c <= 254
-//   E <= 255 * 2^24.  The kernels keep the sums and pack the top bytes of
-//   four of them into one word of codes with byte permutes.
+//   E <= 255 * 2^24.
 //
-//   Signed map (first moment): bucket = |pattern| >> 17 (64 per binade: the
-//   signed thresholds are at least 1.4% apart), clamped to [kSgnLo, kSgnHi]:
-//   magnitudes from 2^-21 (below the smallest nonzero threshold, 5e-7) to
-//   1.016.  Entries [0, kSgnN) are the positive buckets, [kSgnN, 2 kSgnN) the
-//   negative ones.  Every magnitude below 2^-21 shares the first bucket of its
-//   sign; that is exact for all of them but -0.0, whose code (that of +0.0,
-//   128) the kernels obtain by adding +0.0 to a zero quotient first.
-//   Unsigned map (second moment): bucket = pattern >> 16 (128 per binade: its
-//   thresholds are 0.7% apart near 1), clamped to [kUnsLo, kUnsHi] (2^-25,
-//   below the smallest threshold 5e-8, to 1.008), from kUnsOff on.
+//   lookup word.  The kernels look up a word x whose top bits are the
+//   bucket's table index j and whose low bits are low(q), and the table
+//   stores E - j * 2^shift (mod 2^32), so that one add, ent[j] + x, gives
+//   E + low(q) with no masking.  The kernels keep the sums and pack the top
+//   bytes of four of them into one word of codes with byte permutes.
+//
+//   Signed map (first moment): bucket h = |pattern| >> 17 (64 per binade:
+//   the signed thresholds are at least 1.4% apart), clamped to
+//   [kSgnLo, kSgnHi]: magnitudes from 2^-21 (below the smallest nonzero
+//   threshold, 5e-7) to 1.016.  With m the pattern of the clamped magnitude
+//   and s the sign mask of q (all ones when q is negative),
+//       x = m ^ (s & kSgnFlip):
+//   m itself for q >= 0; for q < 0 the low bits complemented and bits 11
+//   and 0 of the bucket flipped.  Every bucket in [kSgnLo, kSgnHi] has bit
+//   11 set, so the negative buckets sit below the positive ones, at
+//   (h ^ 1) - 2^11, and the table spans [kSgnLo - 2^11, kSgnHi] from entry 0
+//   (the indices between the two ranges are never read).  Bit 0 swaps
+//   neighbouring buckets so that the two entries of one magnitude lie
+//   2^11 +- 1 words apart, in different shared-memory banks: 2^11 apart
+//   they share a bank, and a warp holding both signs of one magnitude (a
+//   first moment's usual state) reads them one after the other (per 7B
+//   step with bf16 parameters 12.65 against 12.83 ms, with fp32 ones 13.97
+//   against 14.12).  Every magnitude below 2^-21
+//   shares the first bucket of its sign; that is exact for all of them but
+//   -0.0, whose code (that of +0.0, 128) the kernels obtain by adding +0.0
+//   to a zero quotient first.
+//   Unsigned map (second moment): bucket = pattern >> 16 (128 per binade:
+//   its thresholds are 0.7% apart near 1), clamped to [kUnsLo, kUnsHi]
+//   (2^-25, below the smallest threshold 5e-8, to 1.008), x = the clamped
+//   pattern, entries from kUnsOff on.
 //   Lookups clamp only from below (with fmaxf, which also sends NaN to the
 //   first bucket): a normalised value is a block's own quotient, in [-1, 1]
 //   or NaN (see code_word_signed in kernels.cu), so the bucket of 1.0 is the
-//   top one.
+//   top one.  A clamped value takes the low bits of the clamp, 0 (or all
+//   ones, negative), in a first bucket, which holds no threshold.
 #pragma once
 
 #include <cstddef>
@@ -51,12 +71,20 @@ constexpr uint32_t kSgnShift = 17;                 // signed bucket = |pattern| 
 constexpr uint32_t kSgnLowMask = (1u << kSgnShift) - 1u;
 constexpr uint32_t kSgnLo = 0x1A80u;               // bucket of 2^-21
 constexpr uint32_t kSgnHi = 0x1FC0u;               // bucket of 1.0
-constexpr uint32_t kSgnN = kSgnHi - kSgnLo + 1u;   // buckets per sign
+constexpr uint32_t kSgnNegBit = 0x800u;             // moves negative buckets below the positive ones
+constexpr uint32_t kSgnIdxFlip = kSgnNegBit | 1u;   // bucket bits flipped for q < 0
+constexpr uint32_t kSgnFlip = (kSgnIdxFlip << kSgnShift) | kSgnLowMask;
+constexpr uint32_t kSgnBase = kSgnLo - kSgnNegBit;  // index of entry 0 (lowest negative bucket)
+constexpr uint32_t kSgnSpan = kSgnHi - kSgnBase + 1u;
+static_assert((kSgnLo & ~(kSgnNegBit - 1u)) == (kSgnHi & ~(kSgnNegBit - 1u)) && (kSgnLo & kSgnNegBit),
+              "every signed bucket has bit 11 set");
+static_assert(kSgnLo % 2u == 0u && ((kSgnHi ^ 1u) - kSgnNegBit) < kSgnLo,
+              "negative indices start at kSgnBase and end below the positive ones");
 constexpr uint32_t kUnsShift = 16;                 // unsigned bucket = pattern >> 16
 constexpr uint32_t kUnsLowMask = (1u << kUnsShift) - 1u;
 constexpr uint32_t kUnsLo = 0x3300u;               // pattern >> 16 of 2^-25
 constexpr uint32_t kUnsHi = 0x3F80u;               // pattern >> 16 of 1.0
-constexpr uint32_t kUnsOff = 2u * kSgnN;           // where the unsigned entries start
+constexpr uint32_t kUnsOff = kSgnSpan;             // where the unsigned entries start
 constexpr int kEntries = static_cast<int>((kUnsOff + kUnsHi - kUnsLo + 1u + 3u) / 4u * 4u);
 
 // Index 0: signed map (first moment), 1: unsigned map (second moment).

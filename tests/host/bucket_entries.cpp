@@ -29,20 +29,19 @@ float fbits(uint32_t u) { float f; std::memcpy(&f, &u, 4); return f; }
 uint32_t bits(float f) { uint32_t u; std::memcpy(&u, &f, 4); return u; }
 
 uint32_t lookup_signed(float q, bool* oob) {
-  const uint32_t b = bits(q);
-  const uint32_t h = bits(std::fmax(std::fabs(q), fbits(bwd::kSgnLo << bwd::kSgnShift))) >> bwd::kSgnShift;
-  const uint32_t i = h - bwd::kSgnLo + ((b >> 31) ? bwd::kSgnN : 0u);
-  if (i >= 2 * bwd::kSgnN) { *oob = true; return 0; }
-  const uint32_t low = (b ^ static_cast<uint32_t>(static_cast<int32_t>(b) >> 31)) & bwd::kSgnLowMask;
-  return (g_tab->ent[i] + low) >> bwd::kEntShift;
+  const uint32_t m = bits(std::fmax(std::fabs(q), fbits(bwd::kSgnLo << bwd::kSgnShift)));
+  const uint32_t s = static_cast<uint32_t>(static_cast<int32_t>(bits(q)) >> 31);
+  const uint32_t x = m ^ (s & bwd::kSgnFlip);
+  const uint32_t i = (x >> bwd::kSgnShift) - bwd::kSgnBase;
+  if (i >= bwd::kSgnSpan) { *oob = true; return 0; }
+  return (g_tab->ent[i] + x) >> bwd::kEntShift;
 }
 
 uint32_t lookup_unsigned(float q, bool* oob) {
-  const uint32_t b = bits(q);
-  const uint32_t h = bits(std::fmax(q, fbits(bwd::kUnsLo << bwd::kUnsShift))) >> bwd::kUnsShift;
-  const uint32_t i = bwd::kUnsOff - bwd::kUnsLo + h;
+  const uint32_t x = bits(std::fmax(q, fbits(bwd::kUnsLo << bwd::kUnsShift)));
+  const uint32_t i = bwd::kUnsOff - bwd::kUnsLo + (x >> bwd::kUnsShift);
   if (i < bwd::kUnsOff || i >= static_cast<uint32_t>(bwd::kEntries)) { *oob = true; return 0; }
-  return (g_tab->ent[i] + (b & bwd::kUnsLowMask)) >> bwd::kEntShift;
+  return (g_tab->ent[i] + x) >> bwd::kEntShift;
 }
 
 uint32_t count_le(const float* t, float q) {  // thresholds ascending
