@@ -45,6 +45,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <type_traits>
 
 #include "bwd.h"
 #include "exact_div.cuh"
@@ -61,8 +62,8 @@ constexpr int kQuads = kPer / 4;              // 4-element quads per thread
 constexpr int kSpan = 4 * kGroup;             // elements between a thread's quads
 constexpr int kGroupWarps = kGroup / 32;      // 4
 // Adam: blocks in flight per CTA, one CTA per SM (adam_groups below): seven
-// 128-thread groups (896 threads, 72 registers) with fp32 parameters, six
-// (768 threads, 80 registers) with 16-bit ones.
+// 128-thread groups (896 threads, 72 registers) with fp32 parameters and
+// 16-bit gradients, six (768 threads, 80 registers) otherwise.
 constexpr int kQGroups = 4;                   // blocks in flight per CTA (quantize)
 constexpr int kQCta = kGroup * kQGroups;      // 512 threads
 constexpr int kDeqThreads = 256;              // dequantize: 8 elements per thread
@@ -118,12 +119,13 @@ __device__ __forceinline__ int64_t rem_in_block(int64_t n, int64_t base) {
 
 __device__ __forceinline__ uint32_t byte_of(uint32_t w, int k) { return (w >> (8 * k)) & 0xffu; }
 
-// The same byte by one byte permute (PRMT), which the fused step uses for its
-// dequantizing lookups: 16-bit parameters 12.82 against 13.07 ms per 7B step,
-// fp32 parameters with bf16 gradients (seven groups per SM) 13.98 against
-// 14.13 ms.  Two instantiations keep the shift-and-mask form: fp16 gradients
-// (the permutes spill) and fp32 parameters with fp32 gradients (17.13 against
-// 16.98 ms).
+// The same byte by one byte permute (PRMT), which the fused step uses for
+// its dequantizing lookups in every instantiation but fp32 parameters with
+// fp16 gradients (there 13.79 against 13.68 ms per 7B step).  Elsewhere, ms
+// per 7B step against shifts and masks: 16-bit parameters with bf16
+// gradients 12.82 against 13.07, with fp16 gradients 11.71 against 12.46;
+// fp32 parameters with bf16 gradients 13.98 against 14.13, with fp32
+// gradients 15.98 against 16.90.
 __device__ __forceinline__ uint32_t byte_prmt(uint32_t w, int k) {
   return __byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(k));
 }
@@ -613,14 +615,13 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
   return r;
 }
 
-// Groups per CTA of the fused step.  The DRAM-bound fp32-parameter step runs
-// seven (14.13 against 14.24 ms per 7B step with six; eight spill more and
-// run 14.49).  The issue-bound 16-bit-parameter step: six with bf16
-// parameters, whose 80 registers hold the lookups without spills (seven:
-// 12.43, five: 12.85, against 12.26 ms), seven with fp16 ones (12.20
-// against 12.28 ms with six).
-template <int kP>
-__host__ __device__ constexpr int adam_groups() { return kP == kBF16 ? 6 : 7; }
+// Groups per CTA of the fused step (ms per 7B step).  fp32 parameters with
+// bf16 gradients: seven, 13.83 (six 14.55, eight spill more: 14.1-14.6);
+// fp32 parameters with fp32 gradients: six, 16.92 (seven 17.33); 16-bit
+// parameters: six, bf16 11.69 (seven 12.23, five 12.85 before the split
+// block body), fp16 11.73 (seven 12.17).
+template <int kG, int kP>
+__host__ __device__ constexpr int adam_groups() { return kP == kF32 && kG != kF32 ? 7 : 6; }
 
 // With 16-bit parameters (a step bound by instruction issue) the
 // dequantizing lookups read lane-private copies of both maps: entry c of
@@ -637,9 +638,9 @@ __host__ __device__ constexpr bool adam_rep() { return kP != kF32; }
 template <int kP>
 __host__ __device__ constexpr int adam_smem() { return kTablesBytes + (adam_rep<kP>() ? kRepBytes : 0); }
 
-// The same two numbers for a runtime parameter type (bwd_dtype).
-int adam_groups_of(int p_type) {
-  return p_type == BWD_F32 ? adam_groups<kF32>() : p_type == BWD_BF16 ? adam_groups<kBF16>() : adam_groups<kF16>();
+// The same two numbers for runtime types (bwd_dtype).
+int adam_groups_of(int p_type, int g_type) {
+  return p_type == BWD_F32 && g_type != BWD_F32 ? adam_groups<kBF16, kF32>() : adam_groups<kF32, kF32>();
 }
 int adam_smem_of(int p_type) {
   return p_type == BWD_F32 ? adam_smem<kF32>() : p_type == BWD_BF16 ? adam_smem<kBF16>() : adam_smem<kF16>();
@@ -648,9 +649,9 @@ int adam_smem_of(int p_type) {
 // kG: gradient type; kP: parameter type (kF32, kBF16 or kF16; 16-bit
 // parameters are widened for the update and rounded back on store).
 template <int kG, int kP>
-__global__ void __launch_bounds__(kGroup * adam_groups<kP>(), 1)
+__global__ void __launch_bounds__(kGroup * adam_groups<kG, kP>(), 1)
 adam8bit_kernel(const __grid_constant__ AdamArgs args) {
-  constexpr int kGroups = adam_groups<kP>();
+  constexpr int kGroups = adam_groups<kG, kP>();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   bwd::Tables& tab = *reinterpret_cast<bwd::Tables*>(smem_raw);
   float4* rep4 = reinterpret_cast<float4*>(smem_raw + kTablesBytes);
@@ -731,117 +732,128 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
       }
     }
 
-    float p[kPer], g[kPer];
-    uint32_t mw[kQuads], vw[kQuads];
-    if (vec) {
+    // The block's work, compiled twice: for a full block of a tensor whose
+    // four arrays are 16-byte aligned (vector loads and stores, no branch on
+    // that inside) and for the rest (element-wise, padded).  One branch per
+    // block picks the copy; with the three in-body branches of one shared
+    // copy the step ran 12.22 against 11.66 ms per 7B step with bf16
+    // parameters and 13.96 against 13.83 with fp32 ones.
+    auto body = [&](auto vtag) {
+      constexpr bool kVec = decltype(vtag)::value;
+      float p[kPer], g[kPer];
+      uint32_t mw[kQuads], vw[kQuads];
+      if constexpr (kVec) {
 #pragma unroll
-      for (int k = 0; k < kQuads; ++k) {
-        const int64_t e = base + kSpan * k + 4 * t;
-        load4<kP>(T.p, e, &p[4 * k]);
-        load4<kG>(T.g, e, &g[4 * k]);
-        mw[k] = ld_stream_u1(T.mc + e);
-        vw[k] = ld_stream_u1(T.vc + e);
-      }
-    } else {
-      // padding slots: p = g = 0 and the codes of zero, so m = v = 0 there
-      // and the block absmax is unchanged
-#pragma unroll
-      for (int k = 0; k < kQuads; ++k) {
-        uint32_t cm[4], cv[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int e = slot(t, 4 * k + j);
-          const bool in = e < rem;
-          p[4 * k + j] = in ? load1<kP>(T.p, base + e) : 0.0f;
-          g[4 * k + j] = in ? load1<kG>(T.g, base + e) : 0.0f;
-          cm[j] = in ? T.mc[base + e] : 128u;
-          cv[j] = in ? T.vc[base + e] : 0u;
+        for (int k = 0; k < kQuads; ++k) {
+          const int64_t e = base + kSpan * k + 4 * t;
+          load4<kP>(T.p, e, &p[4 * k]);
+          load4<kG>(T.g, e, &g[4 * k]);
+          mw[k] = ld_stream_u1(T.mc + e);
+          vw[k] = ld_stream_u1(T.vc + e);
         }
-        mw[k] = pack4(cm[0], cm[1], cm[2], cm[3]);
-        vw[k] = pack4(cv[0], cv[1], cv[2], cv[3]);
+      } else {
+        // padding slots: p = g = 0 and the codes of zero, so m = v = 0 there
+        // and the block absmax is unchanged
+#pragma unroll
+        for (int k = 0; k < kQuads; ++k) {
+          uint32_t cm[4], cv[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int e = slot(t, 4 * k + j);
+            const bool in = e < rem;
+            p[4 * k + j] = in ? load1<kP>(T.p, base + e) : 0.0f;
+            g[4 * k + j] = in ? load1<kG>(T.g, base + e) : 0.0f;
+            cm[j] = in ? T.mc[base + e] : 128u;
+            cv[j] = in ? T.vc[base + e] : 0u;
+          }
+          mw[k] = pack4(cm[0], cm[1], cm[2], cm[3]);
+          vw[k] = pack4(cv[0], cv[1], cv[2], cv[3]);
+        }
       }
-    }
 
-    // dequantize -> Adam in fp32, two elements at a time.  The moments take
-    // one rounding per operation in the oracle's order, so they (and the
-    // codes and absmax derived from them) are bit-identical; the parameter
-    // update uses branch-free approximate sqrt and reciprocal (a few ulps
-    // of the update term)
-    float m[kPer], v[kPer];
-    float mx[2] = {0.0f, 0.0f};
-    const float2 ma2 = bwd::dup2(ma_old), va2 = bwd::dup2(va_old), ic2 = bwd::dup2(inv_bc2s);
-    const float2 b1_2 = bwd::dup2(b1), omb1_2 = bwd::dup2(omb1), b2_2 = bwd::dup2(b2), omb2_2 = bwd::dup2(omb2);
-    const float2 eps2 = bwd::dup2(eps), nstep2 = bwd::dup2(-step_size), decay2 = bwd::dup2(decay);
+      // dequantize -> Adam in fp32, two elements at a time.  The moments take
+      // one rounding per operation in the oracle's order, so they (and the
+      // codes and absmax derived from them) are bit-identical; the parameter
+      // update uses branch-free approximate sqrt and reciprocal (a few ulps
+      // of the update term)
+      float m[kPer], v[kPer];
+      float mx[2] = {0.0f, 0.0f};
+      const float2 ma2 = bwd::dup2(ma_old), va2 = bwd::dup2(va_old), ic2 = bwd::dup2(inv_bc2s);
+      const float2 b1_2 = bwd::dup2(b1), omb1_2 = bwd::dup2(omb1), b2_2 = bwd::dup2(b2), omb2_2 = bwd::dup2(omb2);
+      const float2 eps2 = bwd::dup2(eps), nstep2 = bwd::dup2(-step_size), decay2 = bwd::dup2(decay);
 #pragma unroll
-    for (int j = 0; j < kPer; j += 2) {
-      constexpr bool kPerm = kG != kF16 && !(kG == kF32 && kP == kF32);
-      const uint32_t im0 = kPerm ? byte_prmt(mw[j >> 2], j & 3) : byte_of(mw[j >> 2], j & 3);
-      const uint32_t im1 = kPerm ? byte_prmt(mw[j >> 2], (j & 3) + 1) : byte_of(mw[j >> 2], (j & 3) + 1);
-      const uint32_t iv0 = kPerm ? byte_prmt(vw[j >> 2], j & 3) : byte_of(vw[j >> 2], j & 3);
-      const uint32_t iv1 = kPerm ? byte_prmt(vw[j >> 2], (j & 3) + 1) : byte_of(vw[j >> 2], (j & 3) + 1);
-      const float2 mo = bwd::mul2(make_float2(map_s[im0 * kStride], map_s[im1 * kStride]), ma2);
-      const float2 vo = bwd::mul2(make_float2(map_u[iv0 * kStride], map_u[iv1 * kStride]), va2);
-      const float2 g2 = make_float2(g[j], g[j + 1]);
-      // products packed, sums scalar: a packed multiply feeding a packed add
-      // may be contracted into one fused operation, which would change the
-      // rounding
-      const float2 bm = bwd::mul2(b1_2, mo), gm = bwd::mul2(omb1_2, g2);
-      const float2 bv = bwd::mul2(b2_2, vo), gv = bwd::mul2(bwd::mul2(omb2_2, g2), g2);
-      const float2 mm = make_float2(__fadd_rn(bm.x, gm.x), __fadd_rn(bm.y, gm.y));
-      const float2 vv = make_float2(__fadd_rn(bv.x, gv.x), __fadd_rn(bv.y, gv.y));
-      m[j] = mm.x; m[j + 1] = mm.y; v[j] = vv.x; v[j + 1] = vv.y;
-      const float2 den = bwd::fma2(make_float2(sqrt_approx(vv.x), sqrt_approx(vv.y)), ic2, eps2);
-      const float2 rc = make_float2(rcp_approx(den.x), rcp_approx(den.y));
-      const float2 pp = bwd::fma2(bwd::mul2(nstep2, mm), rc, bwd::mul2(make_float2(p[j], p[j + 1]), decay2));
-      p[j] = pp.x; p[j + 1] = pp.y;
-      mx[0] = max3abs(mx[0], mm.x, mm.y);
-      mx[1] = max3(mx[1], vv.x, vv.y);
-    }
-    if (vec) {
-#pragma unroll
-      for (int k = 0; k < kQuads; ++k) {
-        const int64_t e = base + kSpan * k + 4 * t;
-        if (kP != kF32)
-          __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(T.p) + e),
-                 make_uint2(pack16<kP>(p[4 * k], p[4 * k + 1]), pack16<kP>(p[4 * k + 2], p[4 * k + 3])));
-        else
-          __stcs(reinterpret_cast<float4*>(static_cast<float*>(T.p) + e),
-                 make_float4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]));
+      for (int j = 0; j < kPer; j += 2) {
+        constexpr bool kPerm = !(kG == kF16 && kP == kF32);
+        const uint32_t im0 = kPerm ? byte_prmt(mw[j >> 2], j & 3) : byte_of(mw[j >> 2], j & 3);
+        const uint32_t im1 = kPerm ? byte_prmt(mw[j >> 2], (j & 3) + 1) : byte_of(mw[j >> 2], (j & 3) + 1);
+        const uint32_t iv0 = kPerm ? byte_prmt(vw[j >> 2], j & 3) : byte_of(vw[j >> 2], j & 3);
+        const uint32_t iv1 = kPerm ? byte_prmt(vw[j >> 2], (j & 3) + 1) : byte_of(vw[j >> 2], (j & 3) + 1);
+        const float2 mo = bwd::mul2(make_float2(map_s[im0 * kStride], map_s[im1 * kStride]), ma2);
+        const float2 vo = bwd::mul2(make_float2(map_u[iv0 * kStride], map_u[iv1 * kStride]), va2);
+        const float2 g2 = make_float2(g[j], g[j + 1]);
+        // products packed, sums scalar: a packed multiply feeding a packed add
+        // may be contracted into one fused operation, which would change the
+        // rounding
+        const float2 bm = bwd::mul2(b1_2, mo), gm = bwd::mul2(omb1_2, g2);
+        const float2 bv = bwd::mul2(b2_2, vo), gv = bwd::mul2(bwd::mul2(omb2_2, g2), g2);
+        const float2 mm = make_float2(__fadd_rn(bm.x, gm.x), __fadd_rn(bm.y, gm.y));
+        const float2 vv = make_float2(__fadd_rn(bv.x, gv.x), __fadd_rn(bv.y, gv.y));
+        m[j] = mm.x; m[j + 1] = mm.y; v[j] = vv.x; v[j + 1] = vv.y;
+        const float2 den = bwd::fma2(make_float2(sqrt_approx(vv.x), sqrt_approx(vv.y)), ic2, eps2);
+        const float2 rc = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+        const float2 pp = bwd::fma2(bwd::mul2(nstep2, mm), rc, bwd::mul2(make_float2(p[j], p[j + 1]), decay2));
+        p[j] = pp.x; p[j + 1] = pp.y;
+        mx[0] = max3abs(mx[0], mm.x, mm.y);
+        mx[1] = max3(mx[1], vv.x, vv.y);
       }
-    } else {
+      if constexpr (kVec) {
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const int e = slot(t, j);
-        if (e < rem) {
-          if (kP != kF32) static_cast<uint16_t*>(T.p)[base + e] = static_cast<uint16_t>(bits16<kP>(p[j]));
-          else static_cast<float*>(T.p)[base + e] = p[j];
+        for (int k = 0; k < kQuads; ++k) {
+          const int64_t e = base + kSpan * k + 4 * t;
+          if (kP != kF32)
+            __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(T.p) + e),
+                   make_uint2(pack16<kP>(p[4 * k], p[4 * k + 1]), pack16<kP>(p[4 * k + 2], p[4 * k + 3])));
+          else
+            __stcs(reinterpret_cast<float4*>(static_cast<float*>(T.p) + e),
+                   make_float4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int e = slot(t, j);
+          if (e < rem) {
+            if (kP != kF32) static_cast<uint16_t*>(T.p)[base + e] = static_cast<uint16_t>(bits16<kP>(p[j]));
+            else static_cast<float*>(T.p)[base + e] = p[j];
+          }
         }
       }
-    }
 
-    // block absmax of the new moments, then requantize
-    group_max<2>(mx, s_red[group], it & 1, group, t);
-    const float am = mx[0], av = mx[1];
-    quantize_quads<true, false>(m, am, tab, mw);
-    quantize_quads<false, false>(v, av, tab, vw);
-    if (vec) {
+      // block absmax of the new moments, then requantize
+      group_max<2>(mx, s_red[group], it & 1, group, t);
+      const float am = mx[0], av = mx[1];
+      quantize_quads<true, false>(m, am, tab, mw);
+      quantize_quads<false, false>(v, av, tab, vw);
+      if constexpr (kVec) {
 #pragma unroll
-      for (int k = 0; k < kQuads; ++k) {
-        __stcs(reinterpret_cast<unsigned int*>(T.mc + base + kSpan * k) + t, mw[k]);
-        __stcs(reinterpret_cast<unsigned int*>(T.vc + base + kSpan * k) + t, vw[k]);
-      }
-    } else {
+        for (int k = 0; k < kQuads; ++k) {
+          __stcs(reinterpret_cast<unsigned int*>(T.mc + base + kSpan * k) + t, mw[k]);
+          __stcs(reinterpret_cast<unsigned int*>(T.vc + base + kSpan * k) + t, vw[k]);
+        }
+      } else {
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const int e = slot(t, j);
-        if (e < rem) {
-          T.mc[base + e] = static_cast<uint8_t>(byte_of(mw[j >> 2], j & 3));
-          T.vc[base + e] = static_cast<uint8_t>(byte_of(vw[j >> 2], j & 3));
+        for (int j = 0; j < kPer; ++j) {
+          const int e = slot(t, j);
+          if (e < rem) {
+            T.mc[base + e] = static_cast<uint8_t>(byte_of(mw[j >> 2], j & 3));
+            T.vc[base + e] = static_cast<uint8_t>(byte_of(vw[j >> 2], j & 3));
+          }
         }
       }
-    }
-    // every thread of the group read the old absmax before the barrier above
-    if (t == 0) { T.ma[lb] = am; T.va[lb] = av; }
+      // every thread of the group read the old absmax before the barrier above
+      if (t == 0) { T.ma[lb] = am; T.va[lb] = av; }
+    };
+    if (vec) body(std::true_type{});
+    else body(std::false_type{});
   }
 }
 
@@ -982,7 +994,7 @@ bwd_status ensure_device(DeviceState** out) {
     if ((s = occupancy(kd[k], kDeqThreads, 0, &d.occ_dequant[k])) != BWD_OK) return s;
   }
   for (int k = 0; k < 9; ++k)
-    if ((s = occupancy(ka[k], kGroup * adam_groups_of(k / 3), adam_smem_of(k / 3), &d.occ_adam[k])) != BWD_OK)
+    if ((s = occupancy(ka[k], kGroup * adam_groups_of(k / 3, k % 3), adam_smem_of(k / 3), &d.occ_adam[k])) != BWD_OK)
       return s;
   d.ctx = ctx;
   d.ready = true;
@@ -1031,13 +1043,13 @@ void fill_scalars(const bwd_adam_hparams* hp, AdamArgs* a) {
 
 template <int kG, int kP>
 void launch_typed(const AdamArgs& a, int grid, cudaStream_t st) {
-  adam8bit_kernel<kG, kP><<<grid, kGroup * adam_groups<kP>(), adam_smem<kP>(), st>>>(a);
+  adam8bit_kernel<kG, kP><<<grid, kGroup * adam_groups<kG, kP>(), adam_smem<kP>(), st>>>(a);
 }
 
 bwd_status launch_adam_chunk(const AdamArgs& a, int g_type, int p_type, const DeviceState& d, cudaStream_t st) {
   const int64_t total = a.block_start[a.num_tensors];
   if (total == 0) return BWD_OK;
-  const int grid = grid_for(total, adam_groups_of(p_type), d, d.occ_adam[3 * p_type + g_type]);
+  const int grid = grid_for(total, adam_groups_of(p_type, g_type), d, d.occ_adam[3 * p_type + g_type]);
   switch (3 * p_type + g_type) {
     case 0: launch_typed<kF32, kF32>(a, grid, st); break;
     case 1: launch_typed<kBF16, kF32>(a, grid, st); break;
