@@ -700,34 +700,44 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
     const bool vec = T.vec && rem == BWD_BLOCK;
     const float ma_old = T.ma[lb];
     const float va_old = T.va[lb];
-    // four threads ask L2 for the group's next block, one array each, so
-    // that block's loads find it there instead of in DRAM.  With 16-bit
-    // parameters (a step bound by instruction issue) only a next block in
-    // the same tensor is prefetched, which needs no tensor search (13.05
-    // against 13.20 ms per 7B step); with fp32 parameters (bound by DRAM)
-    // the first block of the next tensor is prefetched too (14.24 against
-    // 14.31 ms).
+    // the group asks L2 for its next block, so that block's loads find it
+    // there instead of in DRAM.  With 16-bit parameters (a step bound by
+    // instruction issue) one thread issues the four hints and only a next
+    // block in the same tensor is prefetched, which needs no tensor search
+    // (13.05 against 13.20 ms per 7B step; one thread instead of four, one
+    // array each: 11.47 against 11.69); with fp32 parameters (bound by
+    // DRAM) the first block of the next tensor is prefetched too (14.24
+    // against 14.31 ms), by one thread with 16-bit gradients (13.58 against
+    // 13.82 ms with four) and by four, one array each, with fp32 ones
+    // (15.6 against 16.7 ms with one).
     if (kP != kF32) {
-      if (t < 4) {
+      if (t == 0) {
         const int64_t bn = base + stride * BWD_BLOCK;
         if (T.vec && T.n - bn >= BWD_BLOCK) {
-          if (t == 0) prefetch_l2(static_cast<const char*>(T.p) + bn * elem_bytes<kP>(), BWD_BLOCK * elem_bytes<kP>());
-          else if (t == 1) prefetch_l2(static_cast<const char*>(T.g) + bn * elem_bytes<kG>(), BWD_BLOCK * elem_bytes<kG>());
-          else if (t == 2) prefetch_l2(T.mc + bn, 2048u);
-          else prefetch_l2(T.vc + bn, 2048u);
+          prefetch_l2(static_cast<const char*>(T.p) + bn * elem_bytes<kP>(), BWD_BLOCK * elem_bytes<kP>());
+          prefetch_l2(static_cast<const char*>(T.g) + bn * elem_bytes<kG>(), BWD_BLOCK * elem_bytes<kG>());
+          prefetch_l2(T.mc + bn, 2048u);
+          prefetch_l2(T.vc + bn, 2048u);
         }
       }
-    } else if (t < 4) {
+    } else if (t < (kG == kF32 ? 4 : 1)) {
       const int64_t gn = gb + stride;
       if (gn < total) {
         while (args.block_start[tn + 1] <= gn) ++tn;
         const TensorArgs& N = args.t[tn];
         const int64_t bn = (gn - args.block_start[tn]) * BWD_BLOCK;
         if (N.vec && N.n - bn >= BWD_BLOCK) {
-          if (t == 0) prefetch_l2(static_cast<const char*>(N.p) + bn * elem_bytes<kP>(), BWD_BLOCK * elem_bytes<kP>());
-          else if (t == 1) prefetch_l2(static_cast<const char*>(N.g) + bn * elem_bytes<kG>(), BWD_BLOCK * elem_bytes<kG>());
-          else if (t == 2) prefetch_l2(N.mc + bn, 2048u);
-          else prefetch_l2(N.vc + bn, 2048u);
+          if constexpr (kG == kF32) {
+            if (t == 0) prefetch_l2(static_cast<const char*>(N.p) + bn * elem_bytes<kP>(), BWD_BLOCK * elem_bytes<kP>());
+            else if (t == 1) prefetch_l2(static_cast<const char*>(N.g) + bn * elem_bytes<kG>(), BWD_BLOCK * elem_bytes<kG>());
+            else if (t == 2) prefetch_l2(N.mc + bn, 2048u);
+            else prefetch_l2(N.vc + bn, 2048u);
+          } else {
+            prefetch_l2(static_cast<const char*>(N.p) + bn * elem_bytes<kP>(), BWD_BLOCK * elem_bytes<kP>());
+            prefetch_l2(static_cast<const char*>(N.g) + bn * elem_bytes<kG>(), BWD_BLOCK * elem_bytes<kG>());
+            prefetch_l2(N.mc + bn, 2048u);
+            prefetch_l2(N.vc + bn, 2048u);
+          }
         }
       }
     }

@@ -274,7 +274,7 @@ def test_full_size_gpt_350m_flat_sampled(bwd):
     assert _sampled_full_size(bwd, W.workload("gpt_350m"), blocks_per_tensor=200) > 100
 
 
-@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16, torch.float16])
 def test_adamw_single_step_from_identical_state(bwd, gdt):
     """Decoupled weight decay: p is scaled by 1 - lr*wd before the update."""
     n = 3 * B + 333
@@ -424,7 +424,7 @@ def compare_bf16_params(p_bits, ref_bits):
     assert np.count_nonzero(d) <= max(1e-3 * d.size, 2)
 
 
-@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16, torch.float16])
 def test_bf16_params_step_from_identical_state(bwd, gdt):
     from oracle.adam import round_to_bf16
 
@@ -516,7 +516,7 @@ def test_f16_param_optimizer(bwd):
     assert np.array_equal(st["m_codes"].cpu().numpy(), ref[1]) and np.array_equal(st["v_codes"].cpu().numpy(), ref[3])
 
 
-@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16, torch.float16])
 def test_non_finite_gradients_do_not_fault(bwd, gdt):
     """NaN and infinite gradients (outside the method) in some blocks: the
     step completes and the other blocks are exactly the oracle's."""
