@@ -490,22 +490,44 @@ embed_bwd_runs_kernel(const int64_t* __restrict__ ids, int64_t num_tokens, const
     }
     if (tid == 0) s_nvalid = 0;
     __syncthreads();
-    // bitonic sort of the pairs, ascending by id, then position
-    for (int k = 2; k <= p2; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = tid; i < p2; i += kRThreads) {
-          const int l = i ^ j;
-          if (l > i) {
-            const long long ki = s_key[i], kl = s_key[l];
-            const int pi = s_pos[i], pl = s_pos[l];
-            const bool gt2 = ki > kl || (ki == kl && pi > pl);
-            if (gt2 == ((i & k) == 0)) {
-              s_key[i] = kl; s_key[l] = ki;
-              s_pos[i] = pl; s_pos[l] = pi;
+    // the pairs in ascending order of id, then position.  Up to one key per
+    // thread: rank sort (each thread counts the keys before its own, reading
+    // them as broadcasts; one barrier, against the bitonic network's
+    // log2(p2) (log2(p2) + 1) / 2 barriers: 100.3 against 101-102 us per
+    // 16,384-token backward).  Longer chunks: bitonic sort.
+    if (cnt <= kRThreads) {
+      long long ki = 0;
+      int r = 0;
+      if (tid < cnt) {
+        ki = s_key[tid];
+        for (int j = 0; j < cnt; ++j) {
+          const long long kj = s_key[j];
+          r += (kj < ki || (kj == ki && j < tid)) ? 1 : 0;
+        }
+      }
+      __syncthreads();
+      if (tid < cnt) {
+        s_key[r] = ki;
+        s_pos[r] = tid;
+      }
+      __syncthreads();
+    } else {
+      for (int k = 2; k <= p2; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          for (int i = tid; i < p2; i += kRThreads) {
+            const int l = i ^ j;
+            if (l > i) {
+              const long long ki = s_key[i], kl = s_key[l];
+              const int pi = s_pos[i], pl = s_pos[l];
+              const bool gt2 = ki > kl || (ki == kl && pi > pl);
+              if (gt2 == ((i & k) == 0)) {
+                s_key[i] = kl; s_key[l] = ki;
+                s_pos[i] = pl; s_pos[l] = pi;
+              }
             }
           }
+          __syncthreads();
         }
-        __syncthreads();
       }
     }
     for (int i = tid; i < p2; i += kRThreads)
