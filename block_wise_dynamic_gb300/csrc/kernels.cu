@@ -119,13 +119,12 @@ __device__ __forceinline__ int64_t rem_in_block(int64_t n, int64_t base) {
 
 __device__ __forceinline__ uint32_t byte_of(uint32_t w, int k) { return (w >> (8 * k)) & 0xffu; }
 
-// The same byte by one byte permute (PRMT), which the fused step uses for
-// its dequantizing lookups in every instantiation but fp32 parameters with
-// fp16 gradients (there 13.79 against 13.68 ms per 7B step).  Elsewhere, ms
-// per 7B step against shifts and masks: 16-bit parameters with bf16
-// gradients 12.82 against 13.07, with fp16 gradients 11.71 against 12.46;
-// fp32 parameters with bf16 gradients 13.98 against 14.13, with fp32
-// gradients 15.98 against 16.90.
+// The same byte by one byte permute (PRMT), which the fp32-parameter fused
+// step uses for its dequantizing lookups unless gradients are fp16 (there
+// 13.79 against 13.68 ms per 7B step).  Against shifts and masks, ms per 7B
+// step: bf16 gradients 13.98 against 14.13, fp32 gradients 15.98 against
+// 16.90.  (The 16-bit-parameter step forms its lookup offsets with one
+// permute each too: see its lane-private map copies.)
 __device__ __forceinline__ uint32_t byte_prmt(uint32_t w, int k) {
   return __byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(k));
 }
@@ -625,12 +624,15 @@ __host__ __device__ constexpr int adam_groups() { return kP == kF32 && kG != kF3
 
 // With 16-bit parameters (a step bound by instruction issue) the
 // dequantizing lookups read lane-private copies of both maps: entry c of
-// lane l's copy is word 32 c + l, in bank l, so the 32 lookups of a warp
-// never share a bank (random codes in one 256-word map take about three
-// shared-memory wavefronts per warp lookup): 12.25 against 12.67 ms per 7B
-// step.  The DRAM-bound fp32-parameter step reads the maps themselves (with
-// the copies 14.1 against 13.98 ms).  64 KB beside the 28 KB of tables; one
-// CTA per SM either way.
+// map k for lane l sits at byte 256 c + 128 k + 4 l, in bank l, so the 32
+// lookups of a warp never share a bank (random codes in one 256-word map
+// take about three shared-memory wavefronts per warp lookup: 12.25 against
+// 12.67 ms per 7B step), and one byte permute forms the offset
+// (code << 8) | (lane << 2) from the code word and the lane's offset (with
+// the two maps in separate 32 KB halves, a multiply-add per lookup more:
+// 11.35 against 11.46 ms).  The DRAM-bound fp32-parameter step reads the
+// maps themselves (with the copies 14.1 against 13.98 ms).  64 KB beside
+// the 28 KB of tables; one CTA per SM either way.
 constexpr int kLanes = 32;
 constexpr int kRepBytes = 2 * bwd::kCodes * kLanes * 4;
 template <int kP>
@@ -660,9 +662,8 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
   copy_to_smem(&tab, &g_tables, kTablesBytes);
   __syncthreads();
   if (kRep) {
-    const float* maps = &tab.map[0][0];  // both maps, 2 x 256 contiguous floats
     for (int i = threadIdx.x; i < kRepBytes / 16; i += blockDim.x) {
-      const float v = maps[i >> 3];  // 8 float4 = 32 lanes per entry
+      const float v = tab.map[(i >> 3) & 1][i >> 4];  // 256 B per code: 32 lanes of map 0, then of map 1
       rep4[i] = make_float4(v, v, v, v);
     }
     __syncthreads();
@@ -686,9 +687,10 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
 
   const float b1 = args.b1, omb1 = args.omb1, b2 = args.b2, omb2 = args.omb2;
   const float eps = args.eps, step_size = args.step_size, inv_bc2s = args.inv_bc2s, decay = args.decay;
-  constexpr int kStride = kRep ? kLanes : 1;  // words between a map's entries
-  const float* map_s = kRep ? reinterpret_cast<const float*>(rep4) + (threadIdx.x & (kLanes - 1)) : tab.map[0];
-  const float* map_u = kRep ? map_s + bwd::kCodes * kLanes : tab.map[1];
+  const float* map_s = tab.map[0];
+  const float* map_u = tab.map[1];
+  const unsigned char* const rep_b = reinterpret_cast<const unsigned char*>(rep4);
+  const uint32_t lane4 = (threadIdx.x & (kLanes - 1)) * 4u;
 
   int it = 0;
   for (; gb < total; gb += stride, ++it) {
@@ -793,13 +795,26 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
       const float2 eps2 = bwd::dup2(eps), nstep2 = bwd::dup2(-step_size), decay2 = bwd::dup2(decay);
 #pragma unroll
       for (int j = 0; j < kPer; j += 2) {
-        constexpr bool kPerm = !(kG == kF16 && kP == kF32);
-        const uint32_t im0 = kPerm ? byte_prmt(mw[j >> 2], j & 3) : byte_of(mw[j >> 2], j & 3);
-        const uint32_t im1 = kPerm ? byte_prmt(mw[j >> 2], (j & 3) + 1) : byte_of(mw[j >> 2], (j & 3) + 1);
-        const uint32_t iv0 = kPerm ? byte_prmt(vw[j >> 2], j & 3) : byte_of(vw[j >> 2], j & 3);
-        const uint32_t iv1 = kPerm ? byte_prmt(vw[j >> 2], (j & 3) + 1) : byte_of(vw[j >> 2], (j & 3) + 1);
-        const float2 mo = bwd::mul2(make_float2(map_s[im0 * kStride], map_s[im1 * kStride]), ma2);
-        const float2 vo = bwd::mul2(make_float2(map_u[iv0 * kStride], map_u[iv1 * kStride]), va2);
+        float2 mo, vo;
+        if constexpr (kRep) {
+          // byte offset (code << 8) | (lane << 2) by one permute
+          const uint32_t om0 = __byte_perm(mw[j >> 2], lane4, 0x5504u | ((j & 3) << 4));
+          const uint32_t om1 = __byte_perm(mw[j >> 2], lane4, 0x5504u | (((j & 3) + 1) << 4));
+          const uint32_t ov0 = __byte_perm(vw[j >> 2], lane4, 0x5504u | ((j & 3) << 4));
+          const uint32_t ov1 = __byte_perm(vw[j >> 2], lane4, 0x5504u | (((j & 3) + 1) << 4));
+          mo = bwd::mul2(make_float2(*reinterpret_cast<const float*>(rep_b + om0),
+                                     *reinterpret_cast<const float*>(rep_b + om1)), ma2);
+          vo = bwd::mul2(make_float2(*reinterpret_cast<const float*>(rep_b + 128 + ov0),
+                                     *reinterpret_cast<const float*>(rep_b + 128 + ov1)), va2);
+        } else {
+          constexpr bool kPerm = kG != kF16;
+          const uint32_t im0 = kPerm ? byte_prmt(mw[j >> 2], j & 3) : byte_of(mw[j >> 2], j & 3);
+          const uint32_t im1 = kPerm ? byte_prmt(mw[j >> 2], (j & 3) + 1) : byte_of(mw[j >> 2], (j & 3) + 1);
+          const uint32_t iv0 = kPerm ? byte_prmt(vw[j >> 2], j & 3) : byte_of(vw[j >> 2], j & 3);
+          const uint32_t iv1 = kPerm ? byte_prmt(vw[j >> 2], (j & 3) + 1) : byte_of(vw[j >> 2], (j & 3) + 1);
+          mo = bwd::mul2(make_float2(map_s[im0], map_s[im1]), ma2);
+          vo = bwd::mul2(make_float2(map_u[iv0], map_u[iv1]), va2);
+        }
         const float2 g2 = make_float2(g[j], g[j + 1]);
         // products packed, sums scalar: a packed multiply feeding a packed add
         // may be contracted into one fused operation, which would change the
