@@ -279,13 +279,17 @@ __device__ __forceinline__ void quantize_quads(const float (&x)[kPer], float a, 
 
 // Max over the 128 threads of a group of non-negative values; every thread
 // gets the result.
-// `red` is this group's [2 parities][values][4 warps] scratch.
-template <int kVals>
+// `red` is this group's [2 parities][values][4 warps] scratch.  With
+// kAllLanes every lane stores its warp's (equal) maximum, which needs no
+// branch: the 16-bit-parameter fused step 11.18 against 11.36 ms per 7B
+// step; the fp32-parameter one (13.93 against 13.62) and the signed
+// quantizer (207 against 196 us) run faster with lane 0 alone.
+template <int kVals, bool kAllLanes = false>
 __device__ __forceinline__ void group_max(float (&v)[kVals], float* red, int parity, int group, int t) {
   const int lane = t & 31, warp = t >> 5;
 #pragma unroll
   for (int i = 0; i < kVals; ++i) v[i] = warp_max(v[i]);
-  if (lane == 0) {
+  if (kAllLanes || lane == 0) {
 #pragma unroll
     for (int i = 0; i < kVals; ++i) red[(parity * kVals + i) * kGroupWarps + warp] = v[i];
   }
@@ -854,7 +858,7 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
       }
 
       // block absmax of the new moments, then requantize
-      group_max<2>(mx, s_red[group], it & 1, group, t);
+      group_max<2, kP != kF32>(mx, s_red[group], it & 1, group, t);
       const float am = mx[0], av = mx[1];
       quantize_quads<true, false>(m, am, tab, mw);
       quantize_quads<false, false>(v, av, tab, vw);
