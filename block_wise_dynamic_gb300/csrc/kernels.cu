@@ -120,11 +120,11 @@ __device__ __forceinline__ int64_t rem_in_block(int64_t n, int64_t base) {
 __device__ __forceinline__ uint32_t byte_of(uint32_t w, int k) { return (w >> (8 * k)) & 0xffu; }
 
 // The same byte by one byte permute (PRMT), which the fp32-parameter fused
-// step uses for its dequantizing lookups unless gradients are fp16 (there
-// 13.79 against 13.68 ms per 7B step).  Against shifts and masks, ms per 7B
-// step: bf16 gradients 13.98 against 14.13, fp32 gradients 15.98 against
-// 16.90.  (The 16-bit-parameter step forms its lookup offsets with one
-// permute each too: see its lane-private map copies.)
+// step uses for its dequantizing lookups.  Against shifts and masks, ms per
+// 7B step: bf16 gradients 13.98 against 14.13, fp32 gradients 15.98 against
+// 16.90, fp16 gradients 13.59-13.67 against 14.0-14.3.  (The
+// 16-bit-parameter step forms its lookup offsets with one permute each too:
+// see its lane-private map copies.)
 __device__ __forceinline__ uint32_t byte_prmt(uint32_t w, int k) {
   return __byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(k));
 }
@@ -811,11 +811,8 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
           vo = bwd::mul2(make_float2(*reinterpret_cast<const float*>(rep_b + 128 + ov0),
                                      *reinterpret_cast<const float*>(rep_b + 128 + ov1)), va2);
         } else {
-          constexpr bool kPerm = kG != kF16;
-          const uint32_t im0 = kPerm ? byte_prmt(mw[j >> 2], j & 3) : byte_of(mw[j >> 2], j & 3);
-          const uint32_t im1 = kPerm ? byte_prmt(mw[j >> 2], (j & 3) + 1) : byte_of(mw[j >> 2], (j & 3) + 1);
-          const uint32_t iv0 = kPerm ? byte_prmt(vw[j >> 2], j & 3) : byte_of(vw[j >> 2], j & 3);
-          const uint32_t iv1 = kPerm ? byte_prmt(vw[j >> 2], (j & 3) + 1) : byte_of(vw[j >> 2], (j & 3) + 1);
+          const uint32_t im0 = byte_prmt(mw[j >> 2], j & 3), im1 = byte_prmt(mw[j >> 2], (j & 3) + 1);
+          const uint32_t iv0 = byte_prmt(vw[j >> 2], j & 3), iv1 = byte_prmt(vw[j >> 2], (j & 3) + 1);
           mo = bwd::mul2(make_float2(map_s[im0], map_s[im1]), ma2);
           vo = bwd::mul2(make_float2(map_u[iv0], map_u[iv1]), va2);
         }
