@@ -687,7 +687,7 @@ adam8bit_kernel(const __grid_constant__ AdamArgs args) {
     if (args.block_start[mid] <= gb) lo = mid; else hi = mid - 1;
   }
   int ti = lo;
-  int tn = lo;  // tensor of the block prefetched one iteration ahead (threads 0-3)
+  int tn = lo;  // tensor of the block prefetched one iteration ahead (the prefetching threads)
 
   const float b1 = args.b1, omb1 = args.omb1, b2 = args.b2, omb2 = args.omb2;
   const float eps = args.eps, step_size = args.step_size, inv_bc2s = args.inv_bc2s, decay = args.decay;

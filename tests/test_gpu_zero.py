@@ -55,7 +55,8 @@ def _bits(t):
 
 @pytest.mark.parametrize("world", [2, 3, 8])
 @pytest.mark.parametrize("gdt,pdt", [(torch.bfloat16, torch.float32), (torch.float32, torch.float32),
-                                     (torch.bfloat16, torch.bfloat16)])
+                                     (torch.float16, torch.float32), (torch.bfloat16, torch.bfloat16),
+                                     (torch.float16, torch.float16)])
 def test_sharded_steps_equal_the_unsharded_step(bwd, world, gdt, pdt):
     from block_wise_dynamic_gb300.zero import ShardLayout
 
