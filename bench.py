@@ -475,11 +475,33 @@ def run_ours(args):
         e2e_ms = f0.elapsed_time(f1)
         e2e_step_ms = [fe[k].elapsed_time(fe[k + 1]) for k in range(args.e2e_steps)]
         e2e_ms = max_over_ranks(e2e_ms, dev)
+        # control: the same host<->device copies on the same two streams with
+        # no kernel, per step, right after; a spread here too is the link's
+        h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        fl = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
+        torch.cuda.synchronize(dev)
+        fl[0].record(stream)
+        for k in range(args.e2e_steps):
+            h2d_s.wait_stream(stream)
+            d2h_s.wait_stream(stream)
+            with torch.cuda.stream(h2d_s):
+                for i in range(len(sizes)):
+                    gs[i].copy_(ghv[i], non_blocking=True)
+            with torch.cuda.stream(d2h_s):
+                for i in range(len(sizes)):
+                    phv[i].copy_(ps[i], non_blocking=True)
+            stream.wait_stream(h2d_s)
+            stream.wait_stream(d2h_s)
+            fl[k + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        link_ms = [fl[k].elapsed_time(fl[k + 1]) for k in range(args.e2e_steps)]
         e2e = {"value": world * N * args.e2e_steps / (e2e_ms / 1e3), "unit": "params/s",
                "h2d_bytes_per_step": N * gbytes, "d2h_bytes_per_step": N * pbytes,
                "steps": args.e2e_steps,
                "step_ms": {"min": min(e2e_step_ms), "median": statistics.median(e2e_step_ms),
                            "max": max(e2e_step_ms)},
+               "copies_only_ms": {"min": min(link_ms), "median": statistics.median(link_ms), "max": max(link_ms),
+                                  "what": "the same H2D and D2H copies on two streams, no kernel, per step"},
                "what": "per step through block_wise_dynamic_gb300.offload.PipelinedHostStep: gradients "
                        "H2D from pinned host memory, the 8-bit step, updated fp32 parameters D2H into "
                        "pinned host memory, pipelined over 256 MiB chunks on three streams, after one "
