@@ -224,15 +224,19 @@ def test_optimizer_drop_in_and_exact_resume(bwd):
         assert torch.equal(a, b.detach())
 
 
-def _sampled_full_size(bwd, wl, blocks_per_tensor=2, max_tensors=80, steps=2, seed=0):
+def _sampled_full_size(bwd, wl, blocks_per_tensor=2, max_tensors=80, steps=2, seed=0, pdt=torch.float32):
     """Run the whole workload through one multi-tensor call per step (the
     launch configuration the bench times) and check sampled blocks of the
-    last step against the oracle, from the GPU's own input state."""
+    last step against the oracle, from the GPU's own input state.  With
+    16-bit parameters (pdt) the oracle widens and rounds them back as the
+    kernel does; their values may differ by one unit (compare_bf16_params),
+    the codes and absmax not at all."""
     rng = np.random.default_rng(seed)
     T = len(wl.sizes)
+    p16 = pdt != torch.float32
     ps, gs, sts = [], [], []
     for i, n in enumerate(wl.sizes):
-        ps.append(W.gen_normal(n, 0.02, seed=i, device=DEV))
+        ps.append(W.gen_normal(n, 0.02, seed=i, device=DEV).to(pdt))
         gs.append(W.gen_normal(n, wl.grad_std[i], seed=100_000 + i, device=DEV, dtype=wl.grad_dtype))
         sts.append(bwd.state_init(n, DEV))
     args = bwd.MultiTensorArgs(ps, gs, *[[s[k] for s in sts] for k in range(4)])
@@ -245,7 +249,9 @@ def _sampled_full_size(bwd, wl, blocks_per_tensor=2, max_tensors=80, steps=2, se
         nb = (n + B - 1) // B
         for b in sorted(set([0, nb - 1]) | set(rng.choice(nb, min(nb, blocks_per_tensor), replace=False).tolist())):
             lo, hi = b * B, min(n, (b + 1) * B)
-            inp = (ps[i][lo:hi].cpu().numpy(), g_to_np(gs[i][lo:hi]), sts[i][0][lo:hi].cpu().numpy(),
+            pin = (ps[i][lo:hi].cpu().view(torch.int16).numpy().view(np.uint16) if p16
+                   else ps[i][lo:hi].cpu().numpy())
+            inp = (pin, g_to_np(gs[i][lo:hi]), sts[i][0][lo:hi].cpu().numpy(),
                    sts[i][1][b:b + 1].cpu().numpy(), sts[i][2][lo:hi].cpu().numpy(),
                    sts[i][3][b:b + 1].cpu().numpy())
             samples.append((i, b, lo, hi, inp))
@@ -253,6 +259,14 @@ def _sampled_full_size(bwd, wl, blocks_per_tensor=2, max_tensors=80, steps=2, se
     torch.cuda.synchronize()
     hp = oracle.AdamHParams(lr=wl.lr, step=steps)
     for i, b, lo, hi, inp in samples:
+        if p16:
+            ref = oracle.adam8bit_step(*inp, hp, p_bf16=pdt == torch.bfloat16, p_f16=pdt == torch.float16)
+            compare_bf16_params(ps[i][lo:hi].cpu().view(torch.int16).numpy().view(np.uint16), ref[0],
+                                f16=pdt == torch.float16)
+            got = (sts[i][0][lo:hi], sts[i][1][b:b + 1], sts[i][2][lo:hi], sts[i][3][b:b + 1])
+            for a, r in zip((x.cpu().numpy() for x in got), ref[1:]):
+                assert np.array_equal(a.view(np.uint8), r.view(np.uint8))
+            continue
         ref = oracle.adam8bit_step(*inp, hp)
         got = (ps[i][lo:hi].cpu().numpy(), sts[i][0][lo:hi].cpu().numpy(), sts[i][1][b:b + 1].cpu().numpy(),
                sts[i][2][lo:hi].cpu().numpy(), sts[i][3][b:b + 1].cpu().numpy())
@@ -272,6 +286,14 @@ def test_full_size_ragged_2000_sampled(bwd):
 
 def test_full_size_gpt_350m_flat_sampled(bwd):
     assert _sampled_full_size(bwd, W.workload("gpt_350m"), blocks_per_tensor=200) > 100
+
+
+def test_full_size_llama2_7b_bf16_params_sampled(bwd):
+    assert _sampled_full_size(bwd, W.workload("llama2_7b"), pdt=torch.bfloat16) > 100
+
+
+def test_full_size_gpt_350m_f16_params_sampled(bwd):
+    assert _sampled_full_size(bwd, W.workload("gpt_350m"), blocks_per_tensor=200, pdt=torch.float16) > 100
 
 
 @pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16, torch.float16])
@@ -413,15 +435,27 @@ def test_step_on_tensor_larger_than_2p31_elements(bwd):
     torch.cuda.empty_cache()
 
 
-def compare_bf16_params(p_bits, ref_bits):
-    """bf16 (or fp16) parameters: at most 1e-3 of them one unit apart (the
+def compare_bf16_params(p_bits, ref_bits, f16=False):
+    """bf16 (fp16 with f16) parameters: at most 1e-3 of them differ (the
     fp32 update is within a few ulps, so it can land on the other side of a
-    rounding boundary), none further."""
+    rounding boundary), and those by one unit, unless their values agree
+    within the bound compare_step puts on fp32 parameters, 3e-8 + 4e-7 |p|
+    (inside the required atol 1e-7, rtol 1e-5): a result that cancels to
+    near zero (p + update ~ 0) turns that absolute error into several units
+    of its own small magnitude."""
     a = p_bits.astype(np.int32)
     b = ref_bits.astype(np.int32)
     d = np.abs(a - b)
-    assert d.max(initial=0) <= 1
     assert np.count_nonzero(d) <= max(1e-3 * d.size, 2)
+    far = d > 1
+    if far.any():
+        def val(bits):
+            bits = np.asarray(bits, dtype=np.uint16)
+            if f16:
+                return bits.view(np.float16).astype(np.float64)
+            return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        xa, xb = val(p_bits[far]), val(ref_bits[far])
+        assert np.all(np.abs(xa - xb) <= 3e-8 + 4e-7 * np.abs(xb)), (xa, xb)
 
 
 @pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16, torch.float16])
@@ -493,7 +527,7 @@ def test_f16_params_step_from_identical_state(bwd, gdt):
     for i in range(len(sizes)):
         pb = ps[i].view(torch.int16).numpy().view(np.uint16)
         ref = oracle.adam8bit_step(pb, g_to_np(gs[i]), *sts[i], hp, p_f16=True)
-        compare_bf16_params(dp[i].cpu().view(torch.int16).numpy().view(np.uint16), ref[0])
+        compare_bf16_params(dp[i].cpu().view(torch.int16).numpy().view(np.uint16), ref[0], f16=True)
         for a, b in zip((x.cpu().numpy() for x in dst[i]), ref[1:]):
             assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
 
@@ -512,7 +546,7 @@ def test_f16_param_optimizer(bwd):
         ref = oracle.adam8bit_step(ref[0], widen_f16(g.cpu().view(torch.int16).numpy().view(np.uint16)), *ref[1:],
                                    oracle.AdamHParams(lr=1e-3, step=t), p_f16=True)
     st = opt.state[p]
-    compare_bf16_params(p.detach().cpu().view(torch.int16).numpy().view(np.uint16), ref[0])
+    compare_bf16_params(p.detach().cpu().view(torch.int16).numpy().view(np.uint16), ref[0], f16=True)
     assert np.array_equal(st["m_codes"].cpu().numpy(), ref[1]) and np.array_equal(st["v_codes"].cpu().numpy(), ref[3])
 
 
