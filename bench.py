@@ -598,7 +598,7 @@ def _adam_tensors(wl, pdtype, dev, seed_base=0, grad_dtype=None):
     return sizes, ps, gs, sts
 
 
-def time_adam_workload(name: str, param_dtype: str, dev, steps: int, warmup: int) -> dict:
+def time_adam_workload(name: str, param_dtype: str, dev, steps: int, warmup: int, grad_dtype: str = None) -> dict:
     """One multi-tensor step per timed iteration over a whole workload (as
     the headline line, fewer steps); CUDA events on the launching stream.
     Sets smaller than L2 are timed after an L2 flush per step."""
@@ -608,11 +608,13 @@ def time_adam_workload(name: str, param_dtype: str, dev, steps: int, warmup: int
     from block_wise_dynamic_gb300 import workloads as W
 
     wl = W.workload(name)
-    pdtype = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[param_dtype]
-    sizes, ps, gs, sts = _adam_tensors(wl, pdtype, dev)
+    dts = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+    pdtype = dts[param_dtype]
+    gdtype = dts[grad_dtype] if grad_dtype else wl.grad_dtype
+    sizes, ps, gs, sts = _adam_tensors(wl, pdtype, dev, grad_dtype=gdtype)
     mt = bwd.MultiTensorArgs(ps, gs, *[[s[k] for s in sts] for k in range(4)])
     N = sum(sizes)
-    gbytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
+    gbytes = 4 if gdtype == torch.float32 else 2
     bpp = algorithmic_bytes_per_param(gbytes, 4 if pdtype == torch.float32 else 2)
     flush = bpp * N < 2 * L2_BYTES
     scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
@@ -635,7 +637,8 @@ def time_adam_workload(name: str, param_dtype: str, dev, steps: int, warmup: int
     ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
     peak, _ = measured_peak()
     gbs = bpp * N / (ms / 1e3) / 1e9
-    out = {"workload": name, "param_dtype": param_dtype, "grad_dtype": "bf16" if gbytes == 2 else "f32",
+    out = {"workload": name, "param_dtype": param_dtype,
+           "grad_dtype": {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}[gdtype],
            "tensors": len(sizes), "params": N, "launches_per_step": math.ceil(len(sizes) / 448),
            "steps": steps, "warmup": warmup, "ms_per_step": ms, "params_per_s": N / (ms / 1e3),
            "bytes_per_param": bpp, "gbs": gbs, "frac": gbs / peak,
@@ -757,6 +760,8 @@ def secondary_legs(dev, steps: int = 8, warmup: int = 3) -> dict:
     for name, pdt in (("ragged_2000", "f32"), ("gpt_350m", "f32"), ("adam_1m", "f32"),
                       ("llama2_7b", "bf16"), ("llama2_7b", "f16")):
         legs[f"{name}/p_{pdt}"] = time_adam_workload(name, pdt, dev, steps, warmup)
+    # fp32 parameters with fp16 gradients (fp16 mixed precision)
+    legs["llama2_7b/p_f32_g_f16"] = time_adam_workload("llama2_7b", "f32", dev, steps, warmup, grad_dtype="f16")
     legs["quant_2p28"] = time_quant_passes(dev, steps, warmup)
     return legs
 
